@@ -1,0 +1,224 @@
+"""fp64 CPU oracle for paged KV-cache attention (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product library never does, and the two
+share no code: the arithmetic lives in ``oracle.c`` (plain C, double
+precision), reached here through ``ctypes``.
+
+Every function takes bf16 tensors as their raw 16-bit patterns (``numpy``
+``uint16`` arrays) and returns float64 results.  What each one computes, and
+the passage it follows, is written beside the C function it wraps:
+
+* ``kv_append``      -- bit copy of new K/V rows into pool slots.
+* ``expected_slots`` -- slot = block_table[s][p // B] * B + p % B.
+* ``decode``         -- one query token per sequence over its cached context.
+* ``prefill``        -- causal attention over packed (ragged) prompts, with an
+  optional cached prefix read through the block table.
+* ``mixed_step``     -- append, then decode for the first ``num_decode``
+  sequences and prefill for the rest.
+
+Parity pins: tests/test_oracle_pins.py checks these functions against a
+library routine (torch's scaled-dot-product attention in float64 on dense
+gathered inputs), closed forms and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "oracle.c"
+_BUILD = _HERE / "_build"
+_LIB_PATH = _BUILD / "liboracle.so"
+
+OK = 0
+ERR_SLOT_RANGE = -1
+ERR_SLOT_DUP = -2
+ERR_BLOCK_RANGE = -3
+ERR_ARG = -4
+ERR_NOMEM = -5
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> Path:
+    """Compile oracle.c with gcc into oracle/_build/liboracle.so."""
+    _BUILD.mkdir(exist_ok=True)
+    if (not force and _LIB_PATH.exists()
+            and _LIB_PATH.stat().st_mtime >= _SRC.stat().st_mtime):
+        return _LIB_PATH
+    tmp = _BUILD / f"liboracle.{os.getpid()}.so"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", str(_SRC), "-o", str(tmp), "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(str(build()))
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_kv_append.argtypes = [I, I, I, I, I, P, P, P, P, P]
+        lib.oracle_expected_slots.argtypes = [I, P, P, P, I, I, P]
+        lib.oracle_decode.argtypes = [I, I, I, I, I, I, D, P, P, P, P, I, P, P, I, P, I]
+        lib.oracle_prefill.argtypes = [I, I, I, I, I, I, D, P, P, P, P, P, P, I, P, I, P, I]
+        for f in (lib.oracle_kv_append, lib.oracle_expected_slots,
+                  lib.oracle_decode, lib.oracle_prefill):
+            f.restype = I
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bit patterns as uint16, got {a.dtype}")
+    return a
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        names = {ERR_SLOT_RANGE: "slot out of range", ERR_SLOT_DUP: "duplicate slot",
+                 ERR_BLOCK_RANGE: "block index out of range", ERR_ARG: "bad argument",
+                 ERR_NOMEM: "out of memory"}
+        raise OracleError(f"{what}: {names.get(status, status)}")
+
+
+def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool):
+    """Return copies of (k_pool, v_pool) with the new rows written at their slots.
+
+    k_new/v_new: uint16 [T, Hkv, d]; pools: uint16 [N, Hkv, B, d].
+    """
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    kp, vp = _u16(k_pool).copy(), _u16(v_pool).copy()
+    sm = _i32(slot_mapping)
+    N, Hkv, B, d = kp.shape
+    T = sm.shape[0]
+    assert k_new.shape == (T, Hkv, d) and v_new.shape == (T, Hkv, d)
+    st = _load().oracle_kv_append(T, Hkv, d, B, N, _ptr(k_new), _ptr(v_new), _ptr(sm),
+                                  _ptr(kp), _ptr(vp))
+    _check(st, "kv_append")
+    return kp, vp
+
+
+def expected_slots(q_start_loc, seq_lens, block_table, block_size) -> np.ndarray:
+    qs, sl, bt = _i32(q_start_loc), _i32(seq_lens), _i32(block_table)
+    S = sl.shape[0]
+    out = np.full(int(qs[-1]), -1, dtype=np.int32)
+    st = _load().oracle_expected_slots(S, _ptr(qs), _ptr(sl), _ptr(bt), bt.shape[1],
+                                       block_size, _ptr(out))
+    _check(st, "expected_slots")
+    return out
+
+
+def decode(q, k_pool, v_pool, block_table, seq_lens, scale: float = 0.0,
+           pairs=None, threads: int | None = None) -> np.ndarray:
+    """fp64 decode attention.  q: uint16 [S, Hq, d]; returns float64 [S, Hq, d],
+    or [n, d] for an (s, h) sample list ``pairs`` of shape [n, 2]."""
+    q, kp, vp = _u16(q), _u16(k_pool), _u16(v_pool)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    S, Hq, d = q.shape
+    N, Hkv, B, d2 = kp.shape
+    assert d2 == d and vp.shape == kp.shape and bt.shape[0] >= S and sl.shape[0] == S
+    pr = None if pairs is None else _i32(pairs).reshape(-1, 2)
+    n = S * Hq if pr is None else pr.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    st = _load().oracle_decode(S, Hq, Hkv, d, B, N, float(scale), _ptr(q), _ptr(kp), _ptr(vp),
+                               _ptr(bt), bt.shape[1], _ptr(sl), _ptr(pr),
+                               0 if pr is None else pr.shape[0], _ptr(out),
+                               threads or default_threads())
+    _check(st, "decode")
+    return out.reshape(S, Hq, d) if pr is None else out
+
+
+def prefill(q, k, v, cu_seqlens_q, prefix_lens=None, block_table=None,
+            num_kv_heads: int | None = None, scale: float = 0.0, pairs=None,
+            threads: int | None = None) -> np.ndarray:
+    """fp64 causal prefill over packed prompts.
+
+    Paged form (block_table given): k, v are pools uint16 [N, Hkv, B, d] that
+    already hold every key of the sequence; prefix_lens[s] (default 0) is the
+    number of cached tokens before the prompt rows.
+    Dense form (block_table None): k, v are packed uint16 [T, Hkv, d].
+    Returns float64 [T, Hq, d], or [n, d] for a (row, h) sample list."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    cu = _i32(cu_seqlens_q)
+    S = cu.shape[0] - 1
+    T, Hq, d = q.shape
+    pre = None if prefix_lens is None else _i32(prefix_lens)
+    if block_table is not None:
+        bt = _i32(block_table)
+        N, Hkv, B, d2 = k.shape
+        maxb = bt.shape[1]
+    else:
+        bt = None
+        _, Hkv, d2 = k.shape
+        N, B, maxb = 1, 1, 0
+    assert d2 == d
+    pr = None if pairs is None else _i32(pairs).reshape(-1, 2)
+    n = T * Hq if pr is None else pr.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    st = _load().oracle_prefill(S, Hq, Hkv, d, B, N, float(scale), _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(cu), _ptr(pre), _ptr(bt), maxb, _ptr(pr),
+                                0 if pr is None else pr.shape[0], _ptr(out),
+                                threads or default_threads())
+    _check(st, "prefill")
+    return out.reshape(T, Hq, d) if pr is None else out
+
+
+def mixed_step(q, k_new, v_new, q_start_loc, seq_lens, slot_mapping, block_table,
+               num_decode: int, k_pool, v_pool, scale: float = 0.0,
+               threads: int | None = None):
+    """One continuous-batching step: append every new token, then decode
+    attention for sequences [0, num_decode) (one query row each) and causal
+    prefill with prefix for the rest.  Returns (out float64 [T, Hq, d],
+    k_pool, v_pool) with the pools after the append."""
+    qs, sl, bt = _i32(q_start_loc), _i32(seq_lens), _i32(block_table)
+    kp, vp = kv_append(k_new, v_new, slot_mapping, k_pool, v_pool)
+    q = _u16(q)
+    T, Hq, d = q.shape
+    out = np.zeros((T, Hq, d), dtype=np.float64)
+    nd = int(num_decode)
+    if nd > 0:
+        assert np.all(qs[1:nd + 1] - qs[:nd] == 1)
+        rows = qs[:nd]
+        out[rows] = decode(q[rows], kp, vp, bt[:nd], sl[:nd], scale=scale, threads=threads)
+    S = sl.shape[0]
+    if S > nd:
+        r0, r1 = int(qs[nd]), int(qs[S])
+        cu = qs[nd:] - r0
+        n = cu[1:] - cu[:-1]
+        pre = sl[nd:] - n
+        out[r0:r1] = prefill(q[r0:r1], kp, vp, cu, prefix_lens=pre, block_table=bt[nd:],
+                             scale=scale, threads=threads)
+    return out, kp, vp

@@ -1,0 +1,59 @@
+"""Each plausible mistake planted in a copy of the oracle (on the CPU) must be
+caught by at least one pin; the pins are only worth what they catch."""
+import os
+import subprocess
+import tempfile
+from pathlib import Path
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = Path(oracle.__file__).resolve().parent / "oracle.c"
+
+# (name, original text, replacement, expected count of occurrences)
+MUTATIONS = [
+    ("drop_scale", "x[j] = scale * dot;", "x[j] = dot;", 2),
+    ("gqa_head_mod", "int g = (int)(h / dc->G);", "int g = (int)(h % (dc->Hq / dc->G));", 1),
+    ("prefill_gqa_head_mod", "int g = (int)(h / pc->G);", "int g = (int)(h % (pc->Hq / pc->G));", 1),
+    ("causal_off_by_one", "int L = (int)(p0 + i + 1);", "int L = (int)(p0 + i);", 1),
+    ("no_normalise", "for (int e = 0; e < d; ++e) out[e] /= Z;", "", 2),
+    ("append_swaps_kv", "k_pool[dst + e] = k_new[src + e];", "k_pool[dst + e] = v_new[src + e];", 1),
+    ("v_read_from_k_pool", "const uint16_t *vr = pv->v_pool +", "const uint16_t *vr = pv->k_pool +", 1),
+    ("pool_layout_nhd", "size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off) * head_dim);",
+     "size_t dst = (size_t)(((blk * block_size + off) * num_kv_heads + h) * head_dim);", 1),
+    ("block_offset_wrong", "const uint16_t *kr = pv->k_pool + (size_t)(((long long)blk * H + g) * B + j % B) * d;",
+     "const uint16_t *kr = pv->k_pool + (size_t)(((long long)blk * H + g) * B + (B - 1 - j % B)) * d;", 1),
+    ("prefix_ignored", "int p0 = pc->prefix ? pc->prefix[s] : 0;", "int p0 = 0;", 1),
+    ("default_scale_wrong", "1.0 / sqrt((double)head_dim)", "1.0 / (double)head_dim", 1),
+    ("slot_formula_wrong", "slots_out[q_start[s] + i] = blk * block_size + p % block_size;",
+     "slots_out[q_start[s] + i] = blk * block_size + p / block_size;", 1),
+    ("dup_check_dropped", "if (seen[slot]) { free(seen); return OR_ERR_SLOT_DUP; }", "", 1),
+]
+
+
+def _build_mutant(tmp: Path, orig: str, repl: str, count: int) -> Path:
+    text = SRC.read_text()
+    assert text.count(orig) == count, (orig, text.count(orig))
+    src = tmp / "oracle_mut.c"
+    src.write_text(text.replace(orig, repl))
+    lib = tmp / "liboracle_mut.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+                    str(src), "-o", str(lib), "-lm"], check=True)
+    return lib
+
+
+@pytest.mark.parametrize("name,orig,repl,count", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutant_is_caught(name, orig, repl, count, monkeypatch):
+    with tempfile.TemporaryDirectory() as d:
+        lib = _build_mutant(Path(d), orig, repl, count)
+        monkeypatch.setattr(oracle, "_lib", None)
+        monkeypatch.setattr(oracle, "build", lambda force=False: lib)
+        caught = []
+        for pin in ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError):
+                caught.append(pin.__name__)
+        assert caught, f"mutation {name} passed every pin"
