@@ -1,0 +1,449 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one continuous-batching decode step of the Llama-7B-shaped
+workload (128 running sequences, cached context U[1, 2048], 32 query / 32 KV
+heads, head_dim 128, 16-token blocks, shuffled physical blocks): append each
+sequence's new K/V row into the block pool, then split-K decode attention
+(partial + merge).  Inputs are resident in HBM when the timed region starts;
+the pools (2.4 GB) exceed the 129 MB L2, so no flush is needed between steps.
+
+`value` is the step's algorithmic HBM traffic per second (GB/s): the K/V
+bytes decode must read (sum over sequences of L * Hkv * d * 2 B, K and V),
+q, out, block-table entries and lengths, the split-K partials (written and
+read back), and the append's reads and writes.  The prefill half of the
+metric is measured in the same run on causal prompt batches (the mixed
+step's 8 prompts, 4 x 1024, 1 x 4096; Hq 32 / Hkv 8) and reported in
+TFLOP/s over the unmasked causal pairs only (4 d flops per query head and
+(row, key) pair).
+
+With --impl reference the fp64 CPU oracle runs the same step on the host
+cores (a bounded sample of the sequences per step) and reports the same
+metric.  Under torchrun (N > 1) every rank runs an independent replica
+(weak scaling, no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "paged decode KV-read GB/s (% of HBM peak); prefill attn TFLOP/s (% of peak)"
+WORKLOAD = ("Llama-7B-shaped decode step: 128 running sequences, context U[1,2048] (+1 appended), "
+            "Hq 32 / Hkv 32, head_dim 128, block 16, pool = blocks + 10%, shuffled blocks")
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- workload --
+def decode_step_bytes(shape, seq_lens: np.ndarray, split: int, block_size: int) -> dict:
+    """Algorithmic bytes of one append + decode step."""
+    Hq, Hkv, d = shape.num_q_heads, shape.num_kv_heads, shape.head_dim
+    S = len(seq_lens)
+    L = seq_lens.astype(np.int64)
+    kv = int(L.sum()) * Hkv * d * 2 * 2
+    qo = 2 * S * Hq * d * 2
+    tables = int(np.ceil(L / block_size).sum()) * 4 + S * 4
+    nsplit = np.maximum(1, -(-L // split))
+    multi = nsplit > 1
+    partials = int((nsplit[multi]).sum()) * Hq * (d + 2) * 4 * 2
+    append = S * Hkv * d * 2 * 2 * 2 + S * 4  # read k_new, v_new; write the rows; slots
+    decode = kv + qo + tables + partials
+    return {"kv": kv, "decode": decode, "append": append, "step": decode + append}
+
+
+def causal_flops(prompts, prefix, Hq, d) -> float:
+    tot = 0
+    for n, p in zip(prompts, prefix):
+        tot += n * p + n * (n + 1) // 2  # unmasked (row, key) pairs
+    return 4.0 * d * Hq * tot
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.15)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags) if f == "Active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- distributed --
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max_sum(t_local: float, units_local: float, world: int, device):
+    """Max of the ranks' elapsed times and sum of their units."""
+    if world == 1:
+        return t_local, units_local
+    import torch.distributed as dist
+    t = torch.tensor([t_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------- our arm --
+def run_ours(args, world, rank, local):
+    from paged_kv_cache_continuous_gb300 import binding as pa
+    from paged_kv_cache_continuous_gb300 import workload as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load()
+    hbm_peak, bf16_peak, peak_src = peaks()
+
+    shape, kp, vp, st = wl.llama7b_decode(pool_device=dev)
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
+    q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
+    slots, bt, lens = tod(st.slot_mapping), tod(st.block_table), tod(st.seq_lens)
+    max_len = st.max_seq_len
+    ws = pa.workspace(shape, st.num_seqs, max_len, dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.kv_append(shape, kn, vn, slots, kp, vp)
+        pa.decode(shape, q, kp, vp, bt, lens, max_len, out=out, ws=ws)
+
+    for _ in range(args.warmup):
+        step()
+    pa.check_device_error()
+
+    split, max_splits = pa.decode_plan(shape, st.num_seqs, max_len)
+    nbytes = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
+    launches_per_step = 2 + (1 if max_splits > 1 else 0)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            pa.kv_append(shape, kn, vn, slots, kp, vp)
+            ev[i][1].record(stream)
+            pa.decode(shape, q, kp, vp, bt, lens, max_len, out=out, ws=ws)
+            ev[i][2].record(stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    pa.check_device_error()
+    t_local = e0.elapsed_time(e1) / 1e3
+    t_dec = float(np.mean([a[1].elapsed_time(a[2]) for a in ev])) / 1e3
+    t_app = float(np.mean([a[0].elapsed_time(a[1]) for a in ev])) / 1e3
+    t_max, bytes_all = reduce_max_sum(t_local, nbytes["step"] * K, world, dev)
+    value = bytes_all / t_max / 1e9
+
+    # ---- end to end through the public API with host buffers
+    host = {k: v.cpu().pin_memory() for k, v in dict(q=q, kn=kn, vn=vn, slots=slots, bt=bt, lens=lens).items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+    Ke = max(20, min(K, 500))
+
+    def e2e_step():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        pa.kv_append(shape, dbuf["kn"], dbuf["vn"], dbuf["slots"], kp, vp)
+        pa.decode(shape, dbuf["q"], kp, vp, dbuf["bt"], dbuf["lens"], max_len, out=out, ws=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e, bytes_e2e = reduce_max_sum(s0.elapsed_time(s1) / 1e3, nbytes["step"] * Ke, world, dev)
+
+    # ---- prefill half of the metric (tensor cores), timed alone with L2 flushed
+    prefill = measure_prefill(pa, wl, dev, bf16_peak, peak_src, args.prefill_iters) if rank == 0 else None
+
+    clocks = clk.summary()
+    traffic = load_traffic("decode_splitk", nbytes, st.num_seqs)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(t_max / K * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "num_seqs": st.num_seqs, "num_q_heads": shape.num_q_heads,
+                   "num_kv_heads": shape.num_kv_heads, "head_dim": shape.head_dim,
+                   "block_size": shape.block_size, "num_blocks": shape.num_blocks,
+                   "context_tokens": int(st.seq_lens.sum()), "decode_split_tokens": split,
+                   "l2": "inputs larger than L2 (KV pools 2.4 GB > 129 MB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "decode (decode_splitk_kernel + decode_merge_kernel)",
+                     "achieved": round(nbytes["decode"] / t_dec / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(nbytes["decode"] / t_dec / 1e9 / hbm_peak, 4),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy)",
+                     "frac_of_nominal_8TBps": round(nbytes["decode"] / t_dec / 1e9 / 8000.0, 4),
+                     "traffic": traffic, "algorithmic_bytes": nbytes["decode"],
+                     "kernel_ms": round(t_dec * 1e3, 5)},
+        "append": {"ms": round(t_app * 1e3, 5), "GBps": round(nbytes["append"] / t_app / 1e9, 1)},
+        "e2e": {"value": round(bytes_e2e / t_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "prefill": prefill,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(shape, kp, vp, st, split, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def load_traffic(kernel: str, nbytes, num_seqs):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the
+    current kernel build (profiles/decode_llama7b_traffic.json)."""
+    p = ROOT / "profiles" / "decode_llama7b_traffic.json"
+    if not p.exists():
+        return None
+    try:
+        d = json.loads(p.read_text())
+        src = ROOT / "paged_kv_cache_continuous_gb300" / "csrc" / "decode.cu"
+        import hashlib
+        if d.get("decode_cu_sha256") != hashlib.sha256(src.read_bytes()).hexdigest():
+            return None
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def measure_prefill(pa, wl, dev, bf16_peak, peak_src, iters):
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    res = {}
+    cases = {"mixed-step prompts": None, "4x1024": [1024] * 4, "1x4096": [4096]}
+    for name, prompts in cases.items():
+        if prompts is None:
+            shape, kp, vp, st_m = wl.mixed(pool_device=dev)
+            nd = st_m.num_decode
+            qs = st_m.q_start_loc[nd:] - st_m.q_start_loc[nd]
+            rows = slice(int(st_m.q_start_loc[nd]), int(st_m.q_start_loc[-1]))
+            n = (qs[1:] - qs[:-1]).tolist()
+            q = st_m.q[rows].to(dev)
+            kn, vn = st_m.k_new[rows].to(dev), st_m.v_new[rows].to(dev)
+            slots = torch.from_numpy(st_m.slot_mapping[rows]).to(dev)
+            bt = torch.from_numpy(np.ascontiguousarray(st_m.block_table[nd:])).to(dev)
+            cu = torch.from_numpy(np.ascontiguousarray(qs)).to(dev)
+        else:
+            shape, kp, vp, st_p = wl.prefill_only(60 + len(prompts), prompts, pool_device=dev)
+            n = prompts
+            q, kn, vn = st_p.q.to(dev), st_p.k_new.to(dev), st_p.v_new.to(dev)
+            slots = torch.from_numpy(st_p.slot_mapping).to(dev)
+            bt = torch.from_numpy(st_p.block_table).to(dev)
+            cu = torch.from_numpy(st_p.q_start_loc).to(dev)
+        pa.kv_append(shape, kn, vn, slots, kp, vp)
+        out = torch.empty_like(q)
+        for _ in range(3):
+            pa.prefill(shape, q, kp, vp, cu, max(n), block_table=bt, out=out)
+        pa.check_device_error()
+        times = []
+        for _ in range(iters):
+            flush.add_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            pa.prefill(shape, q, kp, vp, cu, max(n), block_table=bt, out=out)
+            b.record()
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        t = float(np.median([x.elapsed_time(y) for x, y in times])) / 1e3
+        fl = causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim)
+        res[name] = {"prompts": n if len(n) <= 8 else len(n), "ms": round(t * 1e3, 4),
+                     "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / bf16_peak, 4)}
+        del kp, vp
+    best = max(res.values(), key=lambda r: r["tflops"])
+    return {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, TMEM)", "unit": "TFLOP/s",
+            "peak": bf16_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst)",
+            "workloads": res, "achieved_best": best["tflops"], "frac_best": best["frac"],
+            "flops_counted": "4*d*Hq per unmasked causal (row, key) pair", "l2": "flushed (256 MB write) before each launch"}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_step(oracle, shape, kp_h, vp_h, st, seqs, threads):
+    """The oracle's append + decode for the sequences `seqs` of the step."""
+    rows = np.asarray(seqs)
+    kn = st.k_new[rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    vn = st.v_new[rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    qb = st.q[rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    oracle.kv_append(kn, vn, st.slot_mapping[rows], kp_h, vp_h, inplace=True)
+    return oracle.decode(qb, kp_h, vp_h, st.block_table[rows], st.seq_lens[rows], threads=threads)
+
+
+def cpu_sample(st, seconds_budget, per_token_s):
+    """Leading sequences whose decode fits in the time budget (at least 4)."""
+    lens = st.seq_lens.astype(np.int64)
+    est = np.cumsum(lens) * per_token_s
+    k = int(np.searchsorted(est, seconds_budget)) + 1
+    return list(range(max(4, min(k, len(lens)))))
+
+
+def cpu_baseline(shape, kp, vp, st, split, seconds):
+    import oracle
+    threads = oracle.default_threads()
+    kp_h = kp.cpu().view(torch.int16).numpy().view(np.uint16)
+    vp_h = vp.cpu().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle_step(oracle, shape, kp_h, vp_h, st, [0, 1], threads)
+    per_tok = (time.perf_counter() - t0) / max(1, int(st.seq_lens[:2].sum()))
+    seqs = cpu_sample(st, seconds, per_tok)
+    t0 = time.perf_counter()
+    oracle_step(oracle, shape, kp_h, vp_h, st, seqs, threads)
+    t = time.perf_counter() - t0
+    b = decode_step_bytes(shape, st.seq_lens[seqs], split, shape.block_size)["step"]
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"append + decode of the first {len(seqs)} of {st.num_seqs} sequences "
+                      f"({int(st.seq_lens[seqs].sum())} context tokens), fp64, {t:.1f} s"}
+
+
+# --------------------------------------------------------- reference arm --
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_continuous_gb300 import workload as wl
+    oracle.build()
+    shape, kp, vp, st = wl.llama7b_decode(pool_device="cpu")
+    threads = oracle.default_threads()
+    kp_h = kp.view(torch.int16).numpy().view(np.uint16)
+    vp_h = vp.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle_step(oracle, shape, kp_h, vp_h, st, [0, 1], threads)
+    per_tok = (time.perf_counter() - t0) / max(1, int(st.seq_lens[:2].sum()))
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    seqs = cpu_sample(st, budget, per_tok)
+    for _ in range(args.warmup):
+        oracle_step(oracle, shape, kp_h, vp_h, st, seqs, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(oracle, shape, kp_h, vp_h, st, seqs, threads)
+    t = time.perf_counter() - t0
+    b = decode_step_bytes(shape, st.seq_lens[seqs], 512, shape.block_size)["step"] * args.steps
+    v = b / t / 1e9
+    sample = (f"each step: append + decode of the first {len(seqs)} of {st.num_seqs} sequences "
+              f"({int(st.seq_lens[seqs].sum())} context tokens), fp64 oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill-iters", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * pa.h -- libpagedattn: paged KV-cache attention for continuously batched LLM
+ * serving, on one GB300 (sm_103a).
+ *
+ * The problem, as the pages state it (no kernel API is printed there):
+ *  - A router batches requests continuously: new requests join and finished
+ *    ones leave between forward steps (text-generation-inference
+ *    Router/Webserver deep dive, xxmr.cn, sections "Continuous batching" and
+ *    "Simple continuous batching").
+ *  - Each request's past keys and values are cached; the first pass over a
+ *    prompt ("prefill") computes the full causal attention matrix, every later
+ *    pass ("decode") only the new token's attention (same page, section
+ *    "Prefill, Decode and past key values").  Prompts may be chunked and
+ *    concatenated with the running batch (same page, section "the scheduling
+ *    loop from the source").
+ *  - The cache is paged: the router's block allocator hands out fixed-size
+ *    blocks (TGI architecture wiki, data-sketchers.com, section "The Router";
+ *    the v3 schema adds "paged attention support", section "Call Flow").
+ *  - Servers pass ragged batches with index-pointer arrays (Blitzscale docs,
+ *    section "Model": ragged_indptr buffers).
+ *  - Warmup fixes the maximum sizes before serving (TGI architecture wiki,
+ *    section "Call Flow": warmup(max_input_tokens, max_batch_prefill_tokens,
+ *    max_total_tokens, max_batch_size)); pa_workspace_size plays that role.
+ *
+ * Attention is textbook scaled dot-product softmax attention (the plainest
+ * reading; the pages give no formula): query head h reads KV head
+ * h / (Hq / Hkv); scale defaults to 1/sqrt(head_dim).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions shared by every call
+ * ---------------------------------------------------------------------------
+ *  - Pointers named q, k*, v*, out, *_pool, workspace and every int32 index
+ *    array are DEVICE pointers; the caller owns all of them.  The library
+ *    allocates nothing and keeps no state beyond the validation flag, the
+ *    decode split override and a thread-local error message.
+ *  - bf16 everywhere for q, k, v, pools and out; indices are int32.
+ *  - Layouts (row-major, contiguous):
+ *        q        [T][Hq][d]            packed query rows
+ *        k_new    [T][Hkv][d]           packed new keys (values alike)
+ *        k_pool   [N][Hkv][B][d]        block pool ("HND"); v_pool alike
+ *        out      [T][Hq][d]
+ *        block_table [S][max_blocks_per_seq]; entries past a sequence's last
+ *                 block are never read (any value is allowed there)
+ *    Token p of sequence s lives in block block_table[s][p / B], row p % B.
+ *  - d (head_dim) in {64, 128}; B (block_size) in {16, 32}; Hq % Hkv == 0;
+ *    Hq / Hkv <= 16.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) except pa_check_device_error, and returns PA_OK or an
+ *    error code.  Arguments are checked on the host before anything is
+ *    enqueued; on an error nothing is enqueued and pa_last_error() describes
+ *    it.  Indices read on the device (block_table entries, slots, lengths)
+ *    are range-checked by the kernels: an out-of-range value is never
+ *    dereferenced, the affected output is left unspecified and a device error
+ *    word is set, which pa_check_device_error() reports.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG 1   /* null pointer, negative size, bad shape */
+#define PA_ERR_UNSUPPORTED 2   /* head_dim, block_size or head ratio not built */
+#define PA_ERR_WORKSPACE 3     /* workspace missing or smaller than required */
+#define PA_ERR_CUDA 4          /* a CUDA call or kernel launch failed */
+#define PA_ERR_BAD_INDEX 5     /* device saw an out-of-range block, slot or length */
+#define PA_ERR_NO_BLOCKS 6     /* allocator: free list exhausted */
+#define PA_ERR_TIMEOUT 7       /* a bounded device wait gave up */
+
+typedef struct {
+    int num_q_heads;   /* Hq */
+    int num_kv_heads;  /* Hkv; Hq % Hkv == 0 */
+    int head_dim;      /* d: 64 or 128 */
+    int block_size;    /* B: tokens per block, 16 or 32 */
+    int num_blocks;    /* N: blocks in the pool */
+    float scale;       /* softmax scale; 0 means 1/sqrt(head_dim) */
+} pa_shape_t;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int pa_version(void);
+
+/*
+ * Workspace bytes needed by pa_decode / pa_mixed_step for batches of at most
+ * max_seqs sequences whose lengths (after the step's append) are at most
+ * max_seq_len.  The workspace holds split-K partial results (fp32) and is
+ * owned by the caller; its contents need no initialisation.  Writes *bytes.
+ */
+int pa_workspace_size(const pa_shape_t *shape, int max_seqs, int max_seq_len,
+                      size_t *bytes);
+
+/*
+ * Split-K plan of a decode batch (host side, first step of the path): the
+ * tokens per split (a multiple of block_size) and the number of splits of the
+ * longest sequence, for num_seqs sequences of at most max_seq_len tokens on
+ * the current device (its SM count enters the choice).  Sequence s then uses
+ * ceil(seq_lens[s] / split_tokens) splits (1 if it is empty); a sequence with
+ * one split writes its output directly, the others go through the merge.
+ * pa_decode and pa_mixed_step use exactly this plan.
+ */
+int pa_decode_plan(const pa_shape_t *shape, int num_seqs, int max_seq_len,
+                   int *split_tokens, int *max_splits);
+
+/*
+ * KV append (router's slot_mapping contract): for every new token i with
+ * slot = slot_mapping[i] >= 0, copy k_new[i][h][:] to k_pool[slot/B][h][slot%B][:]
+ * and v_new likewise, for all h.  slot < 0 means padding (skipped).  A pure
+ * bit copy.  Slots must be distinct (a repeated slot leaves that row
+ * unspecified); slot >= N*B is skipped and sets the device error word.
+ */
+int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new,
+                 const int32_t *slot_mapping, int num_tokens, void *k_pool,
+                 void *v_pool, void *stream);
+
+/*
+ * Decode attention: one query row per sequence (q [S][Hq][d]) against that
+ * sequence's seq_lens[s] cached tokens (counted after the step's append),
+ * read through block_table.  out [S][Hq][d].  seq_lens[s] == 0 gives zeros.
+ * Long contexts are split into chunks (split-K) whose partial softmax states
+ * are merged by a second kernel; the split is chosen from max_seq_len, which
+ * must bound every seq_lens[s] (a longer sequence sets the device error word).
+ * workspace: at least pa_workspace_size(shape, num_seqs, max_seq_len) bytes.
+ */
+int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool,
+              const void *v_pool, const int32_t *block_table,
+              int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+              int max_seq_len, void *out, void *workspace, size_t ws_bytes,
+              void *stream);
+
+/*
+ * Causal prefill over packed prompts: rows [cu_seqlens_q[s], cu_seqlens_q[s+1])
+ * of q belong to sequence s.  Row i of sequence s sits at absolute position
+ * p0 + i and attends to keys 0 .. p0 + i (bottom-right causal alignment).
+ *  - block_table == NULL: dense form.  k, v are the packed new keys/values
+ *    [T][Hkv][d]; key j of sequence s is row cu_seqlens_q[s] + j; prefix_lens
+ *    must be NULL (p0 = 0).
+ *  - block_table != NULL: paged form.  k, v are the pools; every key of the
+ *    sequence, prefix and new rows alike, is read through block_table (the
+ *    caller appended the new rows first); p0 = prefix_lens[s] (NULL = 0).
+ * num_tokens is the number of rows of q and out (and of k, v in the dense
+ * form); cu_seqlens_q[num_seqs] must not exceed it.  max_q_len bounds every
+ * prompt length (a longer one sets the error word and is not computed).
+ * Runs on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
+ */
+int pa_prefill(const pa_shape_t *shape, const void *q, const void *k,
+               const void *v, const int32_t *cu_seqlens_q,
+               const int32_t *prefix_lens, const int32_t *block_table,
+               int max_blocks_per_seq, int num_seqs, int num_tokens,
+               int max_q_len, void *out, void *stream);
+
+/*
+ * One continuous-batching step (prefill chunks merged into the running batch):
+ *   1. append all num_tokens new rows (k_new/v_new) at slot_mapping;
+ *   2. decode attention for sequences [0, num_decode), which own exactly one
+ *      query row each (q_start_loc[s+1] - q_start_loc[s] == 1);
+ *   3. causal prefill (paged form, prefix = seq_lens[s] - n_s) for sequences
+ *      [num_decode, num_seqs).
+ * q_start_loc [num_seqs+1] packs the rows of q/k_new/v_new/out; seq_lens counts
+ * tokens after the append.  max_seq_len bounds seq_lens, max_q_len bounds the
+ * prefill rows per sequence.  workspace as for pa_decode.
+ */
+int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
+                  const void *v_new, const int32_t *q_start_loc,
+                  const int32_t *seq_lens, const int32_t *slot_mapping,
+                  const int32_t *block_table, int max_blocks_per_seq,
+                  int num_seqs, int num_decode, int num_tokens, int max_seq_len,
+                  int max_q_len, void *k_pool, void *v_pool, void *out,
+                  void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Validation mode (off by default, process-wide).  When on, each call first
+ * runs a bounds-checking pass over block_table/slot_mapping/lengths; if it
+ * finds a bad index it sets the device error word and the call's other
+ * kernels return without touching their outputs.
+ */
+int pa_set_validation(int on);
+
+/*
+ * Synchronises `stream`, reads and clears the device error word of the
+ * current device.  Returns PA_OK, PA_ERR_BAD_INDEX, PA_ERR_TIMEOUT or
+ * PA_ERR_CUDA.
+ */
+int pa_check_device_error(void *stream);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char *pa_last_error(void);
+
+/*
+ * Decode split override (tokens per split; a multiple of block_size), for
+ * tests comparing split and unsplit results.  0 restores the automatic choice.
+ */
+int pa_set_decode_split(int tokens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -114,13 +114,20 @@ def _check(status: int, what: str):
         raise OracleError(f"{what}: {names.get(status, status)}")
 
 
-def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool):
-    """Return copies of (k_pool, v_pool) with the new rows written at their slots.
+def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, inplace: bool = False):
+    """Return (k_pool, v_pool) with the new rows written at their slots:
+    copies, or the given arrays themselves with ``inplace`` (they must then be
+    contiguous uint16 arrays).
 
     k_new/v_new: uint16 [T, Hkv, d]; pools: uint16 [N, Hkv, B, d].
     """
     k_new, v_new = _u16(k_new), _u16(v_new)
-    kp, vp = _u16(k_pool).copy(), _u16(v_pool).copy()
+    if inplace:
+        kp, vp = k_pool, v_pool
+        assert kp.dtype == np.uint16 and vp.dtype == np.uint16
+        assert kp.flags.c_contiguous and vp.flags.c_contiguous
+    else:
+        kp, vp = _u16(k_pool).copy(), _u16(v_pool).copy()
     sm = _i32(slot_mapping)
     N, Hkv, B, d = kp.shape
     T = sm.shape[0]

@@ -1,0 +1,122 @@
+// kv_append.cu -- scatter a step's new K/V rows into the paged block pool,
+// and the optional index-checking pass of validation mode.
+//
+// The router's block allocator owns the blocks (TGI architecture wiki,
+// data-sketchers.com, section "The Router"); the model server only writes
+// each new token's key and value into the slot it was given:
+//     k_pool[slot / B][h][slot % B][:] = k_new[i][h][:]   (v alike)
+// slot < 0 is padding.  A pure bit copy: 16-byte vector loads and stores,
+// consecutive threads on consecutive 16-byte pieces of one (token, head) row,
+// so both the read of k_new and the write into the pool are coalesced.
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+    kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                     const int32_t *__restrict__ slot_mapping, long long num_vec, int vec_per_row,
+                     int num_kv_heads, int block_size, long long num_slots, uint4 *__restrict__ k_pool,
+                     uint4 *__restrict__ v_pool, int *err, int check_err_first) {
+    if (check_err_first && *(volatile int *)err != 0) return;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < num_vec; idx += stride) {
+        const int j = (int)(idx % vec_per_row);             // 16-byte piece within the row
+        const long long th = idx / vec_per_row;             // token * Hkv + head
+        const int h = (int)(th % num_kv_heads);
+        const long long tok = th / num_kv_heads;
+        const int slot = __ldg(slot_mapping + tok);
+        if (slot < 0) continue;
+        if ((long long)slot >= num_slots) {
+            set_error(err, PA_ERR_BAD_INDEX);
+            continue;
+        }
+        const long long blk = slot / block_size, off = slot % block_size;
+        const long long dst = ((blk * num_kv_heads + h) * block_size + off) * vec_per_row + j;
+        const uint4 kv = __ldg(k_new + idx);
+        const uint4 vv = __ldg(v_new + idx);
+        k_pool[dst] = kv;
+        v_pool[dst] = vv;
+    }
+}
+
+// Validation mode: every index the kernels of one call will read is checked
+// here first; a bad one sets the error word (PA_ERR_BAD_INDEX) and the
+// call's other kernels, launched with check_err_first, return untouched.
+__global__ void __launch_bounds__(256) index_check_kernel(const CheckArgs a) {
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    const int nthr = gridDim.x * blockDim.x;
+    const long long num_slots = (long long)a.num_blocks * a.block_size;
+    if (a.slot_mapping)
+        for (int i = tid; i < a.num_tokens; i += nthr) {
+            const int sl = a.slot_mapping[i];
+            if (sl >= 0 && (long long)sl >= num_slots) set_error(a.err, PA_ERR_BAD_INDEX);
+        }
+    for (int s = tid; s < a.num_seqs; s += nthr) {
+        int L = -1;
+        if (a.seq_lens) {
+            L = a.seq_lens[s];
+            if (L < 0 || L > a.max_seq_len) {
+                set_error(a.err, PA_ERR_BAD_INDEX);
+                continue;
+            }
+        }
+        if (a.cu_seqlens) {
+            if (s < a.decode_rows && (a.cu_seqlens[s] != s || a.cu_seqlens[s + 1] != s + 1)) {
+                set_error(a.err, PA_ERR_BAD_INDEX);
+                continue;
+            }
+            const int n = a.cu_seqlens[s + 1] - a.cu_seqlens[s];
+            const int p0 = a.prefix_lens ? a.prefix_lens[s] : (a.seq_lens ? L - n : 0);
+            if (n < 0 || n > a.max_q_len || p0 < 0) {
+                set_error(a.err, PA_ERR_BAD_INDEX);
+                continue;
+            }
+            if (!a.seq_lens) L = p0 + n;
+        }
+        if (a.block_table && L >= 0) {
+            const int nb = (L + a.block_size - 1) / a.block_size;
+            if (nb > a.max_blocks) {
+                set_error(a.err, PA_ERR_BAD_INDEX);
+                continue;
+            }
+            for (int b = 0; b < nb; ++b) {
+                const int blk = a.block_table[(size_t)s * a.max_blocks + b];
+                if (blk < 0 || blk >= a.num_blocks) set_error(a.err, PA_ERR_BAD_INDEX);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
+                             const int32_t *slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks, __nv_bfloat16 *k_pool,
+                             __nv_bfloat16 *v_pool, int *err, int check_err_first,
+                             cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int vec_per_row = head_dim / 8;
+    const long long num_vec = (long long)num_tokens * num_kv_heads * vec_per_row;
+    const int threads = 256;
+    long long blocks = (num_vec + threads - 1) / threads;
+    if (blocks > 152LL * 16) blocks = 152LL * 16;  // grid-stride beyond 16 CTAs per SM
+    kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slot_mapping,
+        num_vec, vec_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size,
+        reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool), err, check_err_first);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_index_check(const CheckArgs &a, cudaStream_t stream) {
+    const int work = a.num_tokens > a.num_seqs ? a.num_tokens : a.num_seqs;
+    int blocks = (work + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 1024) blocks = 1024;
+    index_check_kernel<<<blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,477 @@
+// pa_api.cu -- the C ABI of libpagedattn: argument checks, TMA tensor maps,
+// split planning and kernel launches.  Nothing here allocates device memory;
+// the caller owns every buffer (see include/pa.h for the contract).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <string>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+using namespace pa;
+
+thread_local std::string t_last_error;
+std::atomic<int> g_validation{0};
+std::atomic<int> g_split_override{0};
+
+// Device error word: kernels record PA_ERR_BAD_INDEX / PA_ERR_TIMEOUT here
+// instead of trapping; pa_check_device_error reads and clears it.
+__device__ int g_error_word;
+
+int fail(int code, const std::string &msg) {
+    t_last_error = msg;
+    return code;
+}
+
+int ok() {
+    t_last_error.clear();
+    return PA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(PA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DevState {
+    int *err = nullptr;
+    int num_sms = 0;
+    bool init = false;
+};
+std::mutex g_mu;
+DevState g_dev[64];
+
+int dev_state(DevState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PA_ERR_CUDA, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState &d = g_dev[dev];
+    if (!d.init) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        d.err = static_cast<int *>(p);
+        d.init = true;
+    }
+    *out = &d;
+    return PA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const pa_shape_t *sh) {
+    if (!sh) return fail(PA_ERR_INVALID_ARG, "shape is NULL");
+    if (sh->num_q_heads <= 0 || sh->num_kv_heads <= 0 || sh->num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "head counts and num_blocks must be positive");
+    if (sh->head_dim != 64 && sh->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (sh->block_size != 16 && sh->block_size != 32)
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32");
+    if (sh->num_q_heads % sh->num_kv_heads != 0)
+        return fail(PA_ERR_UNSUPPORTED, "num_q_heads must be a multiple of num_kv_heads");
+    if (sh->num_q_heads / sh->num_kv_heads > 16)
+        return fail(PA_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
+    if (sh->num_kv_heads > 65535 || sh->num_q_heads > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "too many heads");
+    if (!(sh->scale >= 0.f) || std::isinf(sh->scale))
+        return fail(PA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    const long long rows = (long long)sh->num_blocks * sh->num_kv_heads * sh->block_size;
+    if (rows > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "pool too large (rows exceed 2^31)");
+    return PA_OK;
+}
+
+float scale_log2(const pa_shape_t *sh) {
+    const double sc = sh->scale > 0.f ? (double)sh->scale : 1.0 / std::sqrt((double)sh->head_dim);
+    return (float)(sc * 1.4426950408889634);  // log2(e)
+}
+
+// ------------------------------------------------------------ tensor maps --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Pool viewed as [N*Hkv*B rows][d] bf16; box = 64 columns x B rows (one KV
+// block of one head, one 128-byte half of each row), 128-byte swizzle.
+int make_pool_map(CUtensorMap *m, const void *pool, const pa_shape_t *sh) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)sh->head_dim,
+                                (cuuint64_t)sh->num_blocks * sh->num_kv_heads * sh->block_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)sh->head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)sh->block_size};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(pool) failed");
+    return PA_OK;
+}
+
+// Packed rows [T][H][d] bf16; box = 64 columns x 1 head x 128 rows.
+int make_rows_map(CUtensorMap *m, const void *base, int head_dim, int heads, long long rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(rows) failed");
+    return PA_OK;
+}
+
+int split_min_tokens(int block_size) {
+    const int ov = g_split_override.load();
+    const int base = ov > 0 ? ov : 256;
+    return ((base + block_size - 1) / block_size) * block_size;
+}
+
+// ---------------------------------------------------------- the three ops --
+int do_append(const pa_shape_t *sh, const void *k_new, const void *v_new, const int32_t *slots,
+              int num_tokens, void *k_pool, void *v_pool, cudaStream_t st, DevState *d, int check_first) {
+    cudaError_t e = launch_kv_append(static_cast<const __nv_bfloat16 *>(k_new),
+                                     static_cast<const __nv_bfloat16 *>(v_new), slots, num_tokens,
+                                     sh->num_kv_heads, sh->head_dim, sh->block_size, sh->num_blocks,
+                                     static_cast<__nv_bfloat16 *>(k_pool), static_cast<__nv_bfloat16 *>(v_pool),
+                                     d->err, check_first, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return PA_OK;
+}
+
+int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const void *v_pool,
+              const int32_t *block_table, int max_blocks, const int32_t *seq_lens, int num_seqs,
+              int max_seq_len, void *out, void *ws, size_t ws_bytes, cudaStream_t st, DevState *d,
+              int check_first) {
+    const int split = decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len, sh->block_size,
+                                          d->num_sms, g_split_override.load());
+    const int max_splits = decode_max_splits(max_seq_len, split);
+    const size_t need = decode_workspace_bytes(num_seqs, sh->num_q_heads, sh->head_dim, max_splits);
+    if (need > 0 && (ws == nullptr || ws_bytes < need))
+        return fail(PA_ERR_WORKSPACE, "workspace smaller than " + std::to_string(need) + " bytes");
+    if (need > 0 && !aligned16(ws)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    CUtensorMap tk, tv;
+    int rc = make_pool_map(&tk, k_pool, sh);
+    if (rc) return rc;
+    rc = make_pool_map(&tv, v_pool, sh);
+    if (rc) return rc;
+    DecodeArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.part_acc = static_cast<float *>(ws);
+    a.part_ml = need ? static_cast<float *>(ws) + (size_t)num_seqs * sh->num_q_heads * max_splits * sh->head_dim
+                     : nullptr;
+    a.err = d->err;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = sh->num_q_heads;
+    a.num_kv_heads = sh->num_kv_heads;
+    a.group = sh->num_q_heads / sh->num_kv_heads;
+    a.num_blocks = sh->num_blocks;
+    a.max_blocks = max_blocks;
+    a.split_tokens = split;
+    a.max_splits = max_splits;
+    a.max_seq_len = max_seq_len;
+    a.check_err_first = check_first;
+    a.scale_log2 = scale_log2(sh);
+    cudaError_t e = launch_decode(tk, tv, a, sh->head_dim, sh->block_size, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return PA_OK;
+}
+
+int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v, const int32_t *cu,
+               const int32_t *prefix_lens, const int32_t *seq_lens, const int32_t *block_table,
+               int max_blocks, int num_seqs, int num_tokens, int max_q_len, void *out, cudaStream_t st,
+               DevState *d, int check_first) {
+    CUtensorMap tq, tk, tv;
+    int rc = make_rows_map(&tq, q, sh->head_dim, sh->num_q_heads, num_tokens);
+    if (rc) return rc;
+    if (block_table) {
+        rc = make_pool_map(&tk, k, sh);
+        if (!rc) rc = make_pool_map(&tv, v, sh);
+    } else {
+        rc = make_rows_map(&tk, k, sh->head_dim, sh->num_kv_heads, num_tokens);
+        if (!rc) rc = make_rows_map(&tv, v, sh->head_dim, sh->num_kv_heads, num_tokens);
+    }
+    if (rc) return rc;
+    PrefillArgs a{};
+    a.cu_seqlens = cu;
+    a.prefix_lens = prefix_lens;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = d->err;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = sh->num_q_heads;
+    a.num_kv_heads = sh->num_kv_heads;
+    a.group = sh->num_q_heads / sh->num_kv_heads;
+    a.num_blocks = sh->num_blocks;
+    a.max_blocks = max_blocks;
+    a.num_tokens = num_tokens;
+    a.max_q_len = max_q_len;
+    a.num_q_tiles = (max_q_len + 127) / 128;
+    a.check_err_first = check_first;
+    a.scale_log2 = scale_log2(sh);
+    cudaError_t e = launch_prefill(tq, tk, tv, a, sh->head_dim, sh->block_size, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return PA_OK;
+}
+
+int run_check(const CheckArgs &ca, cudaStream_t st) {
+    cudaError_t e = launch_index_check(ca, st);
+    if (e != cudaSuccess) return cuda_fail(e, "index check launch");
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+int pa_workspace_size(const pa_shape_t *shape, int max_seqs, int max_seq_len, size_t *bytes) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is NULL");
+    if (max_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    const int split = split_min_tokens(shape->block_size);
+    *bytes = decode_workspace_bytes(max_seqs, shape->num_q_heads, shape->head_dim,
+                                    decode_max_splits(max_seq_len, split));
+    return ok();
+}
+
+int pa_decode_plan(const pa_shape_t *shape, int num_seqs, int max_seq_len, int *split_tokens,
+                   int *max_splits) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!split_tokens || !max_splits) return fail(PA_ERR_INVALID_ARG, "NULL output pointer");
+    if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    *split_tokens = decode_split_tokens(num_seqs, shape->num_kv_heads, max_seq_len, shape->block_size,
+                                        d->num_sms, g_split_override.load());
+    *max_splits = decode_max_splits(max_seq_len, *split_tokens);
+    return ok();
+}
+
+int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                 int num_tokens, void *k_pool, void *v_pool, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (num_tokens == 0) return ok();
+    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return fail(PA_ERR_INVALID_ARG, "k/v and pools must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.slot_mapping = slot_mapping;
+        ca.num_tokens = num_tokens;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    if ((rc = do_append(shape, k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, st, d, val))) return rc;
+    return ok();
+}
+
+int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
+              const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+              int max_seq_len, void *out, void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_seqs == 0) return ok();
+    if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if ((max_seq_len + shape->block_size - 1) / shape->block_size > max_blocks_per_seq)
+        return fail(PA_ERR_INVALID_ARG, "max_seq_len does not fit in max_blocks_per_seq blocks");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PA_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.block_table = block_table;
+        ca.seq_lens = seq_lens;
+        ca.num_seqs = num_seqs;
+        ca.max_blocks = max_blocks_per_seq;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.max_seq_len = max_seq_len;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                   out, workspace, ws_bytes, st, d, val);
+    if (rc) return rc;
+    return ok();
+}
+
+int pa_prefill(const pa_shape_t *shape, const void *q, const void *k, const void *v, const int32_t *cu_seqlens_q,
+               const int32_t *prefix_lens, const int32_t *block_table, int max_blocks_per_seq, int num_seqs,
+               int num_tokens, int max_q_len, void *out, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_seqs < 0 || num_tokens < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_seqs == 0 || num_tokens == 0 || max_q_len == 0) return ok();
+    if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if (!q || !k || !v || !cu_seqlens_q || !out) return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (!block_table && prefix_lens)
+        return fail(PA_ERR_INVALID_ARG, "prefix_lens needs the paged form (block_table)");
+    if (block_table && max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(PA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.block_table = block_table;
+        ca.cu_seqlens = cu_seqlens_q;
+        ca.prefix_lens = prefix_lens;
+        ca.num_seqs = num_seqs;
+        ca.num_tokens = 0;
+        ca.max_blocks = max_blocks_per_seq;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.max_q_len = max_q_len;
+        ca.max_seq_len = 0x7fffffff;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    rc = do_prefill(shape, q, k, v, cu_seqlens_q, prefix_lens, nullptr, block_table, max_blocks_per_seq,
+                    num_seqs, num_tokens, max_q_len, out, st, d, val);
+    if (rc) return rc;
+    return ok();
+}
+
+int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                  const int32_t *q_start_loc, const int32_t *seq_lens, const int32_t *slot_mapping,
+                  const int32_t *block_table, int max_blocks_per_seq, int num_seqs, int num_decode,
+                  int num_tokens, int max_seq_len, int max_q_len, void *k_pool, void *v_pool, void *out,
+                  void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_seqs < 0 || num_decode < 0 || num_decode > num_seqs || num_tokens < 0 || max_seq_len < 0 ||
+        max_q_len < 0)
+        return fail(PA_ERR_INVALID_ARG, "bad sizes");
+    if (num_seqs == 0) return ok();
+    if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if (num_tokens < num_decode) return fail(PA_ERR_INVALID_ARG, "num_tokens < num_decode");
+    if (!q || !k_new || !v_new || !q_start_loc || !seq_lens || !slot_mapping || !block_table || !k_pool ||
+        !v_pool || !out)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if ((max_seq_len + shape->block_size - 1) / shape->block_size > max_blocks_per_seq)
+        return fail(PA_ERR_INVALID_ARG, "max_seq_len does not fit in max_blocks_per_seq blocks");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(out))
+        return fail(PA_ERR_INVALID_ARG, "q, k/v, pools and out must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.slot_mapping = slot_mapping;
+        ca.num_tokens = num_tokens;
+        ca.block_table = block_table;
+        ca.seq_lens = seq_lens;
+        ca.cu_seqlens = q_start_loc;
+        ca.num_seqs = num_seqs;
+        ca.max_blocks = max_blocks_per_seq;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.max_seq_len = max_seq_len;
+        ca.max_q_len = max_q_len > 1 ? max_q_len : 1;
+        ca.decode_rows = num_decode;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    if (num_tokens > 0 &&
+        (rc = do_append(shape, k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, st, d, val)))
+        return rc;
+    if (num_decode > 0 &&
+        (rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_decode,
+                        max_seq_len, out, workspace, ws_bytes, st, d, val)))
+        return rc;
+    const int np = num_seqs - num_decode;
+    if (np > 0 && max_q_len > 0 && num_tokens > 0)
+        rc = do_prefill(shape, q, k_pool, v_pool, q_start_loc + num_decode, nullptr, seq_lens + num_decode,
+                        block_table + (size_t)num_decode * max_blocks_per_seq, max_blocks_per_seq, np, num_tokens,
+                        max_q_len, out, st, d, val);
+    if (rc) return rc;
+    return ok();
+}
+
+int pa_set_validation(int on) {
+    g_validation.store(on ? 1 : 0);
+    return ok();
+}
+
+int pa_set_decode_split(int tokens) {
+    if (tokens < 0) return fail(PA_ERR_INVALID_ARG, "tokens < 0");
+    g_split_override.store(tokens);
+    return ok();
+}
+
+int pa_check_device_error(void *stream) {
+    DevState *d;
+    int rc = dev_state(&d);
+    if (rc) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    if (word == PA_ERR_BAD_INDEX) return fail(PA_ERR_BAD_INDEX, "device saw an out-of-range index");
+    if (word == PA_ERR_TIMEOUT) return fail(PA_ERR_TIMEOUT, "a bounded device wait gave up");
+    if (word != 0) return fail(PA_ERR_CUDA, "device error word " + std::to_string(word));
+    return ok();
+}
+
+const char *pa_last_error(void) { return t_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// pa_internal.h -- host-side declarations shared by the libpagedattn sources.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// ------------------------------------------------------------- decode ------
+struct DecodeArgs {
+    const __nv_bfloat16 *q;      // [S][Hq][d]
+    const int32_t *block_table;  // [S][max_blocks]
+    const int32_t *seq_lens;     // [S], tokens after the append
+    __nv_bfloat16 *out;          // [S][Hq][d]
+    float *part_acc;             // [S][Hq][max_splits][d], unnormalised sums
+    float *part_ml;              // [S][Hq][max_splits][2]: (max, sum) in log2 units
+    int *err;                    // device error word
+    int num_seqs, num_q_heads, num_kv_heads, group, num_blocks, max_blocks;
+    int split_tokens, max_splits, max_seq_len;
+    int check_err_first;         // validation mode: skip work if *err != 0
+    float scale_log2;            // softmax scale * log2(e)
+};
+
+// Tokens per split-K chunk chosen for a decode batch (multiple of block_size).
+int decode_split_tokens(int num_seqs, int num_kv_heads, int max_seq_len, int block_size,
+                        int num_sms, int override_tokens);
+int decode_max_splits(int max_seq_len, int split_tokens);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits);
+
+cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
+                          int head_dim, int block_size, cudaStream_t stream);
+
+// ------------------------------------------------------------- append ------
+cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
+                             const int32_t *slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks, __nv_bfloat16 *k_pool,
+                             __nv_bfloat16 *v_pool, int *err, int check_err_first,
+                             cudaStream_t stream);
+
+// ------------------------------------------------------------ prefill ------
+struct PrefillArgs {
+    const int32_t *cu_seqlens;   // [S+1] query rows of each sequence (in q/out)
+    const int32_t *prefix_lens;  // [S] or null (0)
+    const int32_t *block_table;  // paged form: [S][max_blocks]; null = dense form
+    const int32_t *seq_lens;     // mixed step: [S] tokens after append (prefix = len - n); or null
+    __nv_bfloat16 *out;          // [T][Hq][d]
+    int *err;
+    int num_seqs, num_q_heads, num_kv_heads, group, num_blocks, max_blocks;
+    int num_tokens;              // rows of q/out (and of packed k/v in the dense form)
+    int max_q_len, num_q_tiles;
+    int check_err_first;
+    float scale_log2;
+};
+
+cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                           const CUtensorMap &tm_v, const PrefillArgs &a, int head_dim,
+                           int block_size, cudaStream_t stream);
+
+// --------------------------------------------------------- validation ------
+struct CheckArgs {
+    const int32_t *slot_mapping;  // [T] or null
+    int num_tokens;
+    const int32_t *block_table;   // [S][max_blocks] or null
+    const int32_t *seq_lens;      // [S] or null
+    const int32_t *cu_seqlens;    // [S+1] or null
+    const int32_t *prefix_lens;   // [S] or null
+    int num_seqs, max_blocks, block_size, num_blocks, max_seq_len, max_q_len;
+    int decode_rows;              // mixed step: sequences [0, decode_rows) own query row s
+    int *err;
+};
+cudaError_t launch_index_check(const CheckArgs &a, cudaStream_t stream);
+
+}  // namespace pa
