@@ -326,12 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < kBN / 8; ++jj) {
                 float p8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p8[e] = fast_exp2(fmaf(x[jj * 8 + e], sl, -mu));
-                    lsum += p8[e];
-                }
+                for (int e = 0; e < 8; ++e) p8[e] = fast_exp2(fmaf(x[jj * 8 + e], sl, -mu));
                 const uint4 pk = make_uint4(pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
                                             pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
+                // Row sums of the same bf16-rounded weights that multiply V.
+                lsum += (bf16x2_sum(pk.x) + bf16x2_sum(pk.y)) + (bf16x2_sum(pk.z) + bf16x2_sum(pk.w));
                 const int hf = jj >> 3, c = jj & 7;
                 *reinterpret_cast<uint4 *>(pb + hf * kTileHalf + r * 128 + ((c ^ (r & 7)) << 4)) = pk;
             }
