@@ -173,6 +173,31 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
                   void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Decode without a caller workspace (no counterpart in the pages: an addition
+ * for callers that cannot allocate device memory, e.g. code running inside a
+ * pre-planned serving loop whose memory is fixed at start-up, or a host that
+ * forbids allocation after warm-up).  Same computation, arguments and layouts
+ * as pa_decode minus the workspace: the split-K partials go to a buffer that
+ * lives inside this library, PA_NOALLOC_SCRATCH_BYTES (16 MiB) of device
+ * memory on every GPU that loads it, held until the process exits.
+ *  - Calls nothing that allocates (no cudaMalloc, no cudaFree).
+ *  - The first call on a device looks up that device's copy of the buffer
+ *    (cudaGetSymbolAddress, with the device current); make that first call
+ *    before any stream capture.
+ *  - A batch whose partials need more than the buffer holds
+ *    (pa_workspace_size(shape, num_seqs, max_seq_len) bytes) is rejected
+ *    with PA_ERR_WORKSPACE before anything is enqueued; use pa_decode then.
+ *  - All calls share the one buffer and nothing in it needs clearing (every
+ *    partial is written before it is read); calls whose kernels overlap on
+ *    the GPU (different streams, no ordering) race on it.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool,
+                      const void *v_pool, const int32_t *block_table,
+                      int max_blocks_per_seq, const int32_t *seq_lens,
+                      int num_seqs, int max_seq_len, void *out, void *stream);
+
+/*
  * Validation mode (off by default, process-wide).  When on, each call first
  * runs a bounds-checking pass over block_table/slot_mapping/lengths; if it
  * finds a bad index it sets the device error word and the call's other

@@ -27,7 +27,8 @@ ERR_TIMEOUT = 7
 
 # Every symbol the two headers declare (checked by the tests).
 EXPORTS = [
-    "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode", "pa_prefill",
+    "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode",
+    "pa_decode_noalloc", "pa_prefill",
     "pa_mixed_step", "pa_set_validation", "pa_check_device_error", "pa_last_error",
     "pa_set_decode_split",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
@@ -72,6 +73,7 @@ def load():
         "pa_decode_plan": ([SP, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
         "pa_kv_append": ([SP, P, P, P, I, P, P, P], I),
         "pa_decode": ([SP, P, P, P, P, I, P, I, I, P, P, S, P], I),
+        "pa_decode_noalloc": ([SP, P, P, P, P, I, P, I, I, P, P], I),
         "pa_prefill": ([SP, P, P, P, P, P, P, I, I, I, I, P, P], I),
         "pa_mixed_step": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P], I),
         "pa_set_validation": ([I], I),
@@ -173,6 +175,20 @@ def decode(shape, q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, ou
                             _bf16(v_pool, "v_pool"), _i32(block_table, "block_table"),
                             int(block_table.shape[1]), _i32(seq_lens, "seq_lens"), S, int(max_seq_len),
                             _bf16(out, "out"), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def decode_noalloc(shape, q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, out=None,
+                   stream=None) -> torch.Tensor:
+    """pa_decode_noalloc: decode with the library's built-in split-K scratch
+    (for callers that cannot allocate a workspace); same result as decode()."""
+    S = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().pa_decode_noalloc(ctypes.byref(_shape(shape)), _bf16(q, "q"), _bf16(k_pool, "k_pool"),
+                                    _bf16(v_pool, "v_pool"), _i32(block_table, "block_table"),
+                                    int(block_table.shape[1]), _i32(seq_lens, "seq_lens"), S,
+                                    int(max_seq_len), _bf16(out, "out"), _stream(stream)))
     return out
 
 

@@ -243,6 +243,30 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
     return PA_OK;
 }
 
+// Split-K scratch for pa_decode_noalloc: a fixed buffer inside the library,
+// one copy per device, so that callers who cannot allocate device memory can
+// still run decode.  Host code must not use the symbol itself as a device
+// address; each device's address is looked up once and cached.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];
+
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PA_ERR_CUDA, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return PA_OK;
+}
+
 int run_check(const CheckArgs &ca, cudaStream_t st) {
     cudaError_t e = launch_index_check(ca, st);
     if (e != cudaSuccess) return cuda_fail(e, "index check launch");
@@ -340,6 +364,54 @@ int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const 
     }
     rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                    out, workspace, ws_bytes, st, d, val);
+    if (rc) return rc;
+    return ok();
+}
+
+int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                      int max_seq_len, void *out, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_seqs == 0) return ok();
+    if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if ((max_seq_len + shape->block_size - 1) / shape->block_size > max_blocks_per_seq)
+        return fail(PA_ERR_INVALID_ARG, "max_seq_len does not fit in max_blocks_per_seq blocks");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PA_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    const int split = decode_split_tokens(num_seqs, shape->num_kv_heads, max_seq_len, shape->block_size,
+                                          d->num_sms, g_split_override.load());
+    const size_t need = decode_workspace_bytes(num_seqs, shape->num_q_heads, shape->head_dim,
+                                               decode_max_splits(max_seq_len, split));
+    if (need > PA_NOALLOC_SCRATCH_BYTES)
+        return fail(PA_ERR_WORKSPACE, "batch needs " + std::to_string(need) +
+                                          " bytes of split-K scratch; the built-in buffer holds " +
+                                          std::to_string(PA_NOALLOC_SCRATCH_BYTES) +
+                                          " (use pa_decode with a caller workspace)");
+    void *scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.block_table = block_table;
+        ca.seq_lens = seq_lens;
+        ca.num_seqs = num_seqs;
+        ca.max_blocks = max_blocks_per_seq;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.max_seq_len = max_seq_len;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                   out, scratch, PA_NOALLOC_SCRATCH_BYTES, st, d, val);
     if (rc) return rc;
     return ok();
 }
