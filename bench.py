@@ -285,10 +285,11 @@ def load_traffic(kernel: str, nbytes, num_seqs):
         return None
     try:
         d = json.loads(p.read_text())
-        src = ROOT / "paged_kv_cache_continuous_gb300" / "csrc" / "decode.cu"
         import hashlib
-        if d.get("decode_cu_sha256") != hashlib.sha256(src.read_bytes()).hexdigest():
-            return None
+        csrc = ROOT / "paged_kv_cache_continuous_gb300" / "csrc"
+        for name, key in (("decode.cu", "decode_cu_sha256"), ("pa_common.cuh", "pa_common_cuh_sha256")):
+            if d.get(key) != hashlib.sha256((csrc / name).read_bytes()).hexdigest():
+                return None  # the kernel changed since the counters were taken
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None

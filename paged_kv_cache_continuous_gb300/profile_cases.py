@@ -1,0 +1,77 @@
+"""Single-kernel cases for profiling (ncu) and quick timing.
+
+    python -m paged_kv_cache_continuous_gb300.profile_cases decode [num_seqs] [llama7b|long]
+    python -m paged_kv_cache_continuous_gb300.profile_cases prefill 4096 | 1024,1024,1024,1024
+    python -m paged_kv_cache_continuous_gb300.profile_cases append
+
+Each case builds its seeded workload on cuda:0, makes three warm-up calls and
+then one more, so `ncu -k regex:<kernel> -s 3 -c 1` captures a warm launch.
+"""
+from __future__ import annotations
+
+import sys
+
+import numpy as np
+import torch
+
+from . import binding as pa
+from . import workload as wl
+
+
+def _d(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda() if isinstance(x, np.ndarray) else x.cuda()
+
+
+def decode(num_seqs: int = 128, which: str = "llama7b"):
+    if which == "long":
+        shape, kp, vp, st = wl.long_context(pool_device="cuda", num_seqs=num_seqs)
+    else:
+        shape, kp, vp, st = wl.llama7b_decode(pool_device="cuda", num_seqs=num_seqs)
+    pa.kv_append(shape, _d(st.k_new), _d(st.v_new), _d(st.slot_mapping), kp, vp)
+    q, bt, lens = _d(st.q), _d(st.block_table), _d(st.seq_lens)
+    ws = pa.workspace(shape, st.num_seqs, st.max_seq_len)
+    out = torch.empty_like(q)
+    for _ in range(4):
+        pa.decode(shape, q, kp, vp, bt, lens, st.max_seq_len, out=out, ws=ws)
+    pa.check_device_error()
+    split, nsplit = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
+    kv = int(st.seq_lens.astype(np.int64).sum()) * shape.num_kv_heads * shape.head_dim * 4
+    print(f"decode {which} seqs={st.num_seqs} split={split} max_splits={nsplit} kv_bytes={kv}")
+
+
+def prefill(prompts):
+    shape, kp, vp, st = wl.prefill_only(64, prompts, pool_device="cuda")
+    pa.kv_append(shape, _d(st.k_new), _d(st.v_new), _d(st.slot_mapping), kp, vp)
+    q, bt, cu = _d(st.q), _d(st.block_table), _d(st.q_start_loc)
+    out = torch.empty_like(q)
+    for _ in range(4):
+        pa.prefill(shape, q, kp, vp, cu, st.max_q_len, block_table=bt, out=out)
+    pa.check_device_error()
+    print(f"prefill prompts={prompts}")
+
+
+def append():
+    shape, kp, vp, st = wl.mixed(pool_device="cuda")
+    kn, vn, sl = _d(st.k_new), _d(st.v_new), _d(st.slot_mapping)
+    for _ in range(4):
+        pa.kv_append(shape, kn, vn, sl, kp, vp)
+    pa.check_device_error()
+    print(f"append tokens={st.num_tokens}")
+
+
+def main(argv):
+    pa.load()
+    torch.cuda.set_device(0)
+    case = argv[1] if len(argv) > 1 else "decode"
+    if case == "decode":
+        decode(int(argv[2]) if len(argv) > 2 else 128, argv[3] if len(argv) > 3 else "llama7b")
+    elif case == "prefill":
+        prefill([int(x) for x in (argv[2] if len(argv) > 2 else "4096").split(",")])
+    elif case == "append":
+        append()
+    else:
+        raise SystemExit(f"unknown case {case}")
+
+
+if __name__ == "__main__":
+    main(sys.argv)
