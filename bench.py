@@ -277,6 +277,77 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
+def run_other_workload(args, local):
+    """Secondary measurements (not the contract line): the long-context decode
+    step (32 x 32K tokens, Hq 64 / Hkv 8) and the mixed continuous-batching
+    step (120 decode sequences + 8 prompts) through pa_mixed_step."""
+    from paged_kv_cache_continuous_gb300 import binding as pa
+    from paged_kv_cache_continuous_gb300 import workload as wl
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load()
+    hbm_peak, bf16_peak, _ = peaks()
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
+
+    def timed(fn, K):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        pa.check_device_error()
+        return a.elapsed_time(b) / 1e3 / K
+
+    res = {"workload": args.workload}
+    if args.workload == "long_context":
+        shape, kp, vp, st = wl.long_context(pool_device=dev)
+        q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
+        slots, bt, lens = tod(st.slot_mapping), tod(st.block_table), tod(st.seq_lens)
+        ws = pa.workspace(shape, st.num_seqs, st.max_seq_len, dev)
+        out = torch.empty_like(q)
+        split, nsplit = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
+        nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
+        t_dec = timed(lambda: pa.decode(shape, q, kp, vp, bt, lens, st.max_seq_len, out=out, ws=ws), args.steps)
+        t_app = timed(lambda: pa.kv_append(shape, kn, vn, slots, kp, vp), args.steps)
+        res.update(decode_ms=round(t_dec * 1e3, 4), decode_GBps=round(nb["decode"] / t_dec / 1e9, 1),
+                   frac_measured=round(nb["decode"] / t_dec / 1e9 / hbm_peak, 4),
+                   frac_nominal=round(nb["decode"] / t_dec / 1e9 / 8000, 4), split=split, splits=nsplit,
+                   append_ms=round(t_app * 1e3, 4))
+    else:
+        shape, kp, vp, st = wl.mixed(pool_device=dev)
+        q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
+        qs, lens, slots, bt = tod(st.q_start_loc), tod(st.seq_lens), tod(st.slot_mapping), tod(st.block_table)
+        nd = st.num_decode
+        ws = pa.workspace(shape, nd, st.max_seq_len, dev)
+        out = torch.empty_like(q)
+        step = lambda: pa.mixed_step(shape, q, kn, vn, qs, lens, slots, bt, nd, st.max_seq_len, st.max_q_len,
+                                     kp, vp, out=out, ws=ws)
+        t_step = timed(step, args.steps)
+        split, _ = pa.decode_plan(shape, nd, int(st.seq_lens[:nd].max()))
+        nb = decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)
+        n = (st.q_start_loc[nd + 1:] - st.q_start_loc[nd:-1]).tolist()
+        fl = causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim)
+        # the two halves alone, for comparison with the merged step
+        qd, btd, lensd = q[:nd], bt[:nd], lens[:nd]
+        t_dec = timed(lambda: pa.decode(shape, qd, kp, vp, btd.contiguous(), lensd.contiguous(),
+                                        int(st.seq_lens[:nd].max()), ws=ws), args.steps)
+        r0 = int(st.q_start_loc[nd])
+        qp = q[r0:].contiguous()
+        cup = (qs[nd:] - r0).contiguous()
+        btp = bt[nd:].contiguous()
+        t_pre = timed(lambda: pa.prefill(shape, qp, kp, vp, cup, st.max_q_len, block_table=btp), args.steps)
+        res.update(step_ms=round(t_step * 1e3, 4), decode_alone_ms=round(t_dec * 1e3, 4),
+                   prefill_alone_ms=round(t_pre * 1e3, 4), decode_kv_GB=round(nb["kv"] / 1e9, 4),
+                   prefill_GFLOP=round(fl / 1e9, 2), prefill_rows=int(sum(n)),
+                   decode_GBps_alone=round(nb["decode"] / t_dec / 1e9, 1),
+                   prefill_TFLOPs_alone=round(fl / t_pre / 1e12, 1))
+    print(json.dumps(res), flush=True)
+
+
 def load_traffic(kernel: str, nbytes, num_seqs):
     """DRAM bytes per launch from the committed ncu summary, if it matches the
     current kernel build (profiles/decode_llama7b_traffic.json)."""
@@ -433,6 +504,8 @@ def main():
     ap.add_argument("--prefill-iters", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["llama7b_decode", "long_context", "mixed"], default="llama7b_decode",
+                    help="llama7b_decode prints the contract line; the others print secondary measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -442,6 +515,9 @@ def main():
             import torch.distributed as dist
             dist.init_process_group("gloo")
         run_reference(args, world, rank)
+        return
+    if args.workload != "llama7b_decode":
+        run_other_workload(args, local)
         return
     if world > 1:
         import torch.distributed as dist

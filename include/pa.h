@@ -160,6 +160,10 @@ int pa_prefill(const pa_shape_t *shape, const void *q, const void *k,
  *      query row each (q_start_loc[s+1] - q_start_loc[s] == 1);
  *   3. causal prefill (paged form, prefix = seq_lens[s] - n_s) for sequences
  *      [num_decode, num_seqs).
+ * Steps 2 and 3 run concurrently: the prefill goes to a higher-priority
+ * stream owned by the library (one per device, created on first use), forked
+ * from `stream` after the append and joined back into it with events, so work
+ * enqueued on `stream` afterwards sees the whole step.
  * q_start_loc [num_seqs+1] packs the rows of q/k_new/v_new/out; seq_lens counts
  * tokens after the append.  max_seq_len bounds seq_lens, max_q_len bounds the
  * prefill rows per sequence.  workspace as for pa_decode.

@@ -267,6 +267,37 @@ int noalloc_scratch(void **out) {
     return PA_OK;
 }
 
+// Mixed step: the prefill half runs on a second, higher-priority stream of
+// the library's own, forked from and joined back into the caller's stream
+// with events, so the tensor-bound prefill CTAs and the HBM-bound decode CTAs
+// share the GPU instead of running back to back.  One side stream and one
+// event pair per device, created on first use; the mutex keeps concurrent
+// callers' fork/join sequences from interleaving.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+int side_stream(SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PA_ERR_CUDA, "device ordinal out of range");
+    SideStream &s = g_side[dev];
+    if (!s.stream) {
+        int lo = 0, hi = 0;
+        e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "creating the mixed-step side stream");
+    }
+    *out = &s;
+    return PA_OK;
+}
+
 int run_check(const CheckArgs &ca, cudaStream_t st) {
     cudaError_t e = launch_index_check(ca, st);
     if (e != cudaSuccess) return cuda_fail(e, "index check launch");
@@ -502,16 +533,35 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
     if (num_tokens > 0 &&
         (rc = do_append(shape, k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, st, d, val)))
         return rc;
-    if (num_decode > 0 &&
-        (rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_decode,
-                        max_seq_len, out, workspace, ws_bytes, st, d, val)))
-        return rc;
     const int np = num_seqs - num_decode;
-    if (np > 0 && max_q_len > 0 && num_tokens > 0)
-        rc = do_prefill(shape, q, k_pool, v_pool, q_start_loc + num_decode, nullptr, seq_lens + num_decode,
-                        block_table + (size_t)num_decode * max_blocks_per_seq, max_blocks_per_seq, np, num_tokens,
-                        max_q_len, out, st, d, val);
-    if (rc) return rc;
+    const bool has_prefill = np > 0 && max_q_len > 0 && num_tokens > 0;
+    auto prefill_on = [&](cudaStream_t s) {
+        return do_prefill(shape, q, k_pool, v_pool, q_start_loc + num_decode, nullptr, seq_lens + num_decode,
+                          block_table + (size_t)num_decode * max_blocks_per_seq, max_blocks_per_seq, np,
+                          num_tokens, max_q_len, out, s, d, val);
+    };
+    auto decode_on = [&](cudaStream_t s) {
+        return do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_decode,
+                         max_seq_len, out, workspace, ws_bytes, s, d, val);
+    };
+    if (num_decode > 0 && has_prefill) {
+        std::lock_guard<std::mutex> lk(g_side_mu);
+        SideStream *side;
+        if ((rc = side_stream(&side))) return rc;
+        cudaError_t e = cudaEventRecord(side->fork, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "forking the mixed step");
+        rc = prefill_on(side->stream);
+        const int rc2 = decode_on(st);
+        e = cudaEventRecord(side->join, side->stream);  // join even after a failed launch
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "joining the mixed step");
+        if (rc) return rc;
+        if (rc2) return rc2;
+        return ok();
+    }
+    if (num_decode > 0 && (rc = decode_on(st))) return rc;
+    if (has_prefill && (rc = prefill_on(st))) return rc;
     return ok();
 }
 
