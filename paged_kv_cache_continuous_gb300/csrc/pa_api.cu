@@ -131,13 +131,14 @@ int make_pool_map(CUtensorMap *m, const void *pool, const pa_shape_t *sh) {
     return PA_OK;
 }
 
-// Packed rows [T][H][d] bf16; box = 64 columns x 1 head x 128 rows.
-int make_rows_map(CUtensorMap *m, const void *base, int head_dim, int heads, long long rows) {
+// Packed rows [T][H][d] bf16; box = 64 columns x 1 head x box_rows rows.
+int make_rows_map(CUtensorMap *m, const void *base, int head_dim, int heads, long long rows,
+                  int box_rows = 128) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
-    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     const cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -216,7 +217,8 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
         rc = make_pool_map(&tk, k, sh);
         if (!rc) rc = make_pool_map(&tv, v, sh);
     } else {
-        rc = make_rows_map(&tk, k, sh->head_dim, sh->num_kv_heads, num_tokens);
+        const int kbox = sh->head_dim == 128 ? 64 : 128;  // CTA pairs load half-tiles of K
+        rc = make_rows_map(&tk, k, sh->head_dim, sh->num_kv_heads, num_tokens, kbox);
         if (!rc) rc = make_rows_map(&tv, v, sh->head_dim, sh->num_kv_heads, num_tokens);
     }
     if (rc) return rc;
@@ -238,7 +240,8 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
     a.num_q_tiles = (max_q_len + 127) / 128;
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
-    cudaError_t e = launch_prefill(tq, tk, tv, a, sh->head_dim, sh->block_size, st);
+    cudaError_t e = sh->head_dim == 128 ? launch_prefill_pair(tq, tk, tv, a, sh->block_size, st)
+                                        : launch_prefill(tq, tk, tv, a, sh->head_dim, sh->block_size, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PA_OK;
 }

@@ -58,6 +58,12 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                            const CUtensorMap &tm_v, const PrefillArgs &a, int head_dim,
                            int block_size, cudaStream_t stream);
 
+// head_dim 128 on CTA pairs (M = 256 tcgen05.mma).  Dense form: tm_k boxes
+// are 64 rows (each CTA of the pair loads half of a 128-key tile).
+cudaError_t launch_prefill_pair(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                const CUtensorMap &tm_v, const PrefillArgs &a,
+                                int block_size, cudaStream_t stream);
+
 // --------------------------------------------------------- validation ------
 struct CheckArgs {
     const int32_t *slot_mapping;  // [T] or null

@@ -32,7 +32,7 @@ def test_prefill_dense_tiny(cuda_lib):
     assert_close(out, ref, "tiny dense prefill")
 
 
-@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (16, 16, 128), (16, 2, 64)])
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (16, 16, 128), (8, 4, 128), (24, 8, 128), (16, 2, 64)])
 def test_prefill_dense_ragged(cuda_lib, Hq, Hkv, d):
     lens = [1, 7, 127, 128, 129, 300, 513]
     shape, q, k, v, cu = _dense_case(21, lens, Hq, Hkv, d)
@@ -56,7 +56,8 @@ def _paged_case(seed, prefix_and_new, Hq, Hkv, d, B):
     return shape, kp, vp, st, np.array([p for p, _ in prefix_and_new], dtype=np.int32)
 
 
-@pytest.mark.parametrize("Hq,Hkv,d,B", [(32, 8, 128, 16), (32, 8, 128, 32), (8, 8, 64, 16), (64, 8, 128, 16)])
+@pytest.mark.parametrize("Hq,Hkv,d,B", [(32, 8, 128, 16), (32, 8, 128, 32), (16, 8, 128, 16), (12, 12, 128, 32),
+                                         (8, 8, 64, 16), (64, 8, 128, 16)])
 def test_prefill_paged_with_prefix(cuda_lib, Hq, Hkv, d, B):
     case = [(0, 1), (5, 200), (130, 129), (1000, 64), (17, 300), (0, 256)]
     shape, kp, vp, st, pre = _paged_case(22, case, Hq, Hkv, d, B)
