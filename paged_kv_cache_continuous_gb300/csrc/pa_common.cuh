@@ -310,6 +310,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
         : "memory");
 }
 
+// 16 registers -> 16 consecutive TMEM columns, without waiting: several
+// stores may be in flight; tmem_wait_st() waits for all of them.
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 64 consecutive TMEM columns of this thread's lane -> 64 registers (one
 // load instruction and one wait).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
@@ -469,11 +484,23 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
 
 // Arrive on the mbarrier at this offset in both CTAs of the pair once every
 // MMA issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
+// D(TMEM) (+)= A(TMEM) * B(smem) for a CTA pair: each CTA supplies the A rows
+// of its own TMEM lanes at the same column address.
+__device__ __forceinline__ void umma_bf16_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                      uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, unsigned short cta_mask = 3) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
-        "h"((unsigned short)3)
+        "h"(cta_mask)
         : "memory");
 }
 

@@ -8,10 +8,11 @@
 // position p0 + i and
 //     out = softmax(scale * q K^T + causal mask) V   over keys 0 .. p0 + i.
 //
-// Why pairs: on one SM a 128x128x16 tcgen05.mma with both operands in shared
-// memory costs ~133 SM cycles however small N is, ~46 % of the per-clock dense
-// peak; the same instruction issued for a CTA pair (M = 256, cta_group::2)
-// costs ~73 cycles and does twice the work, ~84 % of peak per SM.
+// Why pairs: a lone SM reaches the dense tensor peak with 128x128x16 MMAs
+// too, but then every MMA also streams all of B (K or V) from its own shared
+// memory; shared-memory bandwidth (operand reads + TMA writes) is what bounds
+// this kernel.  An M = 256 instruction issued once for two SMs (cta_group::2)
+// reads half of B in each CTA, and each CTA loads half of every K/V tile.
 //
 // Work unit: a CTA pair owns four 128-row query tiles that read the same KV
 // head -- four query heads of one group (group size a multiple of 4), two
@@ -22,12 +23,18 @@
 //     along N between the pair), both 64-column halves of d.
 //   V tile (128 keys): CTA c loads all keys, d columns 64c .. 64c+63.
 //   S_k = Q_k K^T (M=256, N=128, K=128) -> each CTA's TMEM S_k (128 columns).
-//   Softmax (thread = row = TMEM lane) writes P_k (bf16) to shared memory in
-//     the 128-byte-swizzled K-major layout, then arrives on the leader.
-//   O_k += P_k V (M=256, N=128: the two d halves, K=128 keys) -> TMEM O_k.
-// Warps: 0-3 and 4-7 softmax for sub-tiles 0 and 1 (warp q: rows 32q ..
-// 32q+31, all 128 columns); 8 TMA producer; 9 TMEM allocation (both CTAs)
-// and, in the leader CTA only, the MMA issuer.
+//   Softmax (thread = row = TMEM lane) writes P_k (bf16 pairs) over the first
+//     64 columns of S_k, then arrives on the leader.
+//   O_k += P_k V (A from TMEM, M=256, N=128: the two d halves, K=128 keys).
+//   The leader issues, per KV tile, PV_0(t), S_0(t+1), PV_1(t), S_1(t+1): while
+//   the tensor core works for one sub-tile the other's softmax runs.  S_k(t+1)
+//   overwrites P_k(t) and so waits for PV_k(t) (in-order tensor pipe).
+// Warps: 0 and 1 issue (leader CTA only) the MMAs of sub-tiles 0 and 1 -- a
+// thread stalls for hundreds of cycles on each mbarrier test, and the other
+// thread's queued MMAs keep the tensor core busy meanwhile; warp 0 also
+// allocates TMEM (both CTAs); 2 TMA producer; 3-6 and 7-10 softmax for
+// sub-tiles 0 and 1 (warp w: rows 32 (w % 4) .. +31, TMEM lane quadrant
+// w % 4, all 128 columns).
 // Loads signal the leader's barriers (cp.async.bulk.tensor .cta_group::2);
 // the leader's commits signal both CTAs (multicast).  The last V tile is
 // loaded against a local barrier in each CTA so its rows past the last key can
@@ -45,21 +52,22 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBM = 128;                       // rows per query sub-tile (per CTA)
 constexpr int kBN = 128;                       // keys per KV tile
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMmaWarp = 0;       // and kMmaWarp + 1
+constexpr int kProducerWarp = 2;
+constexpr int kSoftmaxWarp0 = 3;
+constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;            // S_0, S_1, O_0, O_1
 constexpr int kBox = 128 * 128;                // one [128 rows][64 bf16] swizzled box set
 constexpr int kQBytes = 2 * kBox;              // Q_k: [128][128]
-constexpr int kPBytes = 2 * kBox;              // P_k: [128 rows][128 keys]
 constexpr int kKHalf = 64 * 128;               // [64 keys][64 d]
-constexpr int kSlotBytes = 2 * kKHalf;         // K: 64 keys x 128 d; V: 128 keys x 64 d
+constexpr int kKBytes = 2 * kKHalf;            // K: 64 keys x 128 d (per CTA)
+constexpr int kVBytes = 128 * 128;             // V: 128 keys x 64 d (per CTA)
+constexpr int kStageBytes = kKBytes + kVBytes; // one KV tile: K then V
 constexpr int kQOff = 0;
-constexpr int kPOff = 2 * kQBytes;
-constexpr int kRingOff = kPOff + 2 * kPBytes;
-constexpr int kSlots = 6;
-constexpr int kBarOff = kRingOff + kSlots * kSlotBytes;
-constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2;
+constexpr int kRingOff = 2 * kQBytes;
+constexpr int kStages = 5;                     // K/V ring: five tiles
+constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 4 + 2;
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
 
 struct RowTile {
@@ -93,13 +101,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                 ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *q_full = bar;
-    uint64_t *slot_full = bar + 1;
-    uint64_t *slot_free = slot_full + kSlots;
-    uint64_t *s_full = slot_free + kSlots;  // [2]
-    uint64_t *p_full = s_full + 2;          // [2] leader: 8 arrivals (the softmax warps of both CTAs)
-    uint64_t *o_done = p_full + 2;          // [2]
-    uint64_t *v_last = o_done + 2;          // local: this CTA's half of the last V tile landed
+    uint64_t *tile_full = bar + 1;          // [kStages] leader: K and V of a tile landed in both CTAs
+    uint64_t *tile_free = tile_full + kStages;  // [kStages] both sub-tiles' MMAs on the tile have completed
+    uint64_t *s_full = tile_free + kStages; // [2] S_k(t) is in TMEM (commit, both CTAs)
+    uint64_t *p_full = s_full + 2;          // [2] leader: P_k(t) stored by the 8 softmax warps of the pair
+    uint64_t *o_done = p_full + 2;          // [2] the last PV_k has completed (commit, both CTAs)
+    uint64_t *v_last = o_done + 2;         // local: this CTA's half of the last V tile landed
     uint64_t *v_tail = v_last + 1;          // leader: both halves zeroed past the last key
+    uint64_t *mma_fin = v_tail + 1;         // [2] leader: every MMA issued by thread k has completed
+    uint64_t *turn = mma_fin + 2;           // [2] leader: issuing thread k has queued its j-th group
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bar + kNumBars);
     int *s_abort = reinterpret_cast<int *>(s_tmem + 1);
 
@@ -143,9 +153,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&slot_full[i], 1);
-            mbar_init(&slot_free[i], 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&tile_full[i], 1);
+            mbar_init(&tile_free[i], 2);  // one commit per issuing thread (two if one sub-tile reads the tile)
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&s_full[k], 1);
@@ -154,6 +164,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(v_last, 1);
         mbar_init(v_tail, 2);
+        mbar_init(&mma_fin[0], 1);
+        mbar_init(&mma_fin[1], 1);
+        mbar_init(&turn[0], 1);
+        mbar_init(&turn[1], 1);
         // Validation mode: the leader's reading of the error word decides for
         // both CTAs (it may change while the kernel runs).
         *s_abort = (a.check_err_first && *(volatile int *)a.err != 0) ? 1 : 0;
@@ -191,164 +205,171 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_load_3d_pair(smem + kQOff + k * kQBytes + hf * kBox, &tm_q, lq, hf * 64, mine[k].h,
                                      row0 + mine[k].q0);
         }
-        for (int t = 0; t < T; ++t) {
-            int rows_of[kBPT];  // pool row of each block of this tile (or past the pool)
-            if (PAGED) {
-                const int bi = t * kBPT + lane;
-                int row = oob_row;
-                if (lane < kBPT && bi < nb_used) {
-                    int blk = bt[bi];
-                    if ((unsigned)blk >= (unsigned)a.num_blocks) {
-                        set_error(a.err, PA_ERR_BAD_INDEX);
-                        blk = 0;  // never dereference an out-of-range block
-                    }
-                    row = (blk * a.num_kv_heads + g) * BS;
+        // Pool rows of the tiles' blocks: lane l holds block 32 j + l of lane
+        // group j (kTPG tiles); the next group's entries are loaded while the
+        // current group is issued.  Each TMA copy of a tile is issued by its
+        // own lane.
+        constexpr int kTPG = 32 / kBPT;
+        auto block_row = [&](int bi) {
+            int row = oob_row;
+            if (bi < nb_used) {
+                int blk = bt[bi];
+                if ((unsigned)blk >= (unsigned)a.num_blocks) {
+                    set_error(a.err, PA_ERR_BAD_INDEX);
+                    blk = 0;  // never dereference an out-of-range block
                 }
-#pragma unroll
-                for (int jb = 0; jb < kBPT; ++jb) rows_of[jb] = __shfl_sync(0xffffffffu, row, jb);
+                row = (blk * a.num_kv_heads + g) * BS;
             }
-            const bool last_v = (t == T - 1);
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const int i = 2 * t + kv;
-                const int slot = i % kSlots;
-                uint8_t *dst = smem + kRingOff + slot * kSlotBytes;
-                bool ok = true;
-                if (lane == 0 && i >= kSlots) ok = mbar_wait(&slot_free[slot], ((i / kSlots) - 1) & 1, a.err);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok || *(volatile int *)s_abort) {
-                    if (lane == 0) atomicExch(s_abort, 1);
-                    break;
+            return row;
+        };
+        int row_cur = 0, row_nxt = 0;
+        if (PAGED) {
+            row_cur = block_row(lane);
+            row_nxt = block_row(32 + lane);
+        }
+        for (int t = 0; t < T; ++t) {
+            if (PAGED && t > 0 && t % kTPG == 0) {
+                row_cur = row_nxt;
+                row_nxt = block_row((t / kTPG + 1) * 32 + lane);
+            }
+            const int base = (t % kTPG) * kBPT;
+            const int st = t % kStages;
+            uint8_t *dk = smem + kRingOff + st * kStageBytes;
+            uint8_t *dv = dk + kKBytes;
+            bool ok = true;
+            if (lane == 0 && t >= kStages) ok = mbar_wait(&tile_free[st], ((t / kStages) - 1) & 1, a.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok || *(volatile int *)s_abort) {
+                if (lane == 0) atomicExch(s_abort, 1);
+                break;
+            }
+            const bool last = (t == T - 1);
+            const uint32_t lb = map_to_cta(smem_u32(&tile_full[st]), 0);
+            if (lane == 0 && c == 0) mbar_arrive_expect_tx(&tile_full[st], last ? 2 * kKBytes : 2 * kStageBytes);
+            // K: this CTA's 64 keys, both halves of d (lane = 2 block + half)
+            const int jb = (lane >> 1) & (64 / BS - 1), hf = lane & 1;
+            const int krow = PAGED ? __shfl_sync(0xffffffffu, row_cur, base + c * (64 / BS) + jb) : 0;
+            if (PAGED) {
+                if (lane < 2 * (64 / BS)) tma_load_2d_pair(dk + hf * kKHalf + jb * BS * 128, &tm_k, lb, hf * 64, krow);
+            } else if (lane < 2) {
+                tma_load_3d_pair(dk + hf * kKHalf, &tm_k, lb, hf * 64, g, row0 + t * kBN + 64 * c);
+            }
+            // V: all 128 keys, this CTA's half of d (lane = block)
+            const int vrow = PAGED ? __shfl_sync(0xffffffffu, row_cur, base + (lane & (kBPT - 1))) : 0;
+            if (!last) {
+                if (PAGED) {
+                    if (lane < kBPT) tma_load_2d_pair(dv + lane * BS * 128, &tm_v, lb, c * 64, vrow);
+                } else if (lane == 0) {
+                    tma_load_3d_pair(dv, &tm_v, lb, c * 64, g, row0 + t * kBN);
                 }
-                if (kv == 0) {
-                    // K: this CTA's 64 keys, both halves of d
-                    if (lane == 0) {
-                        const uint32_t lb = map_to_cta(smem_u32(&slot_full[slot]), 0);
-                        if (c == 0) mbar_arrive_expect_tx(&slot_full[slot], 2 * kSlotBytes);
-                        if (PAGED) {
-#pragma unroll
-                            for (int jb = 0; jb < 64 / BS; ++jb)
-#pragma unroll
-                                for (int hf = 0; hf < 2; ++hf)
-                                    tma_load_2d_pair(dst + hf * kKHalf + jb * BS * 128, &tm_k, lb, hf * 64,
-                                                     c == 0 ? rows_of[jb] : rows_of[64 / BS + jb]);
-                        } else {
-#pragma unroll
-                            for (int hf = 0; hf < 2; ++hf)
-                                tma_load_3d_pair(dst + hf * kKHalf, &tm_k, lb, hf * 64, g, row0 + t * kBN + 64 * c);
-                        }
-                    }
-                } else if (!last_v) {
-                    // V: all 128 keys, this CTA's half of d
-                    if (lane == 0) {
-                        const uint32_t lb = map_to_cta(smem_u32(&slot_full[slot]), 0);
-                        if (c == 0) mbar_arrive_expect_tx(&slot_full[slot], 2 * kSlotBytes);
-                        if (PAGED) {
-#pragma unroll
-                            for (int jb = 0; jb < kBPT; ++jb)
-                                tma_load_2d_pair(dst + jb * BS * 128, &tm_v, lb, c * 64, rows_of[jb]);
-                        } else {
-                            tma_load_3d_pair(dst, &tm_v, lb, c * 64, g, row0 + t * kBN);
-                        }
-                    }
-                } else {
-                    // The last V tile: land it against a local barrier, zero
-                    // its rows past the last key, then tell the leader.
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(v_last, kSlotBytes);
-                        if (PAGED) {
-#pragma unroll
-                            for (int jb = 0; jb < kBPT; ++jb)
-                                tma_load_2d(dst + jb * BS * 128, &tm_v, v_last, c * 64, rows_of[jb]);
-                        } else {
-                            tma_load_3d(dst, &tm_v, v_last, c * 64, g, row0 + t * kBN);
-                        }
-                    }
-                    const bool vok = __all_sync(0xffffffffu, mbar_wait(v_last, 0, a.err));
-                    if (vok) {
-                        const int valid = kv_end_max - t * kBN;
-                        for (int r = valid + (lane >> 3); r < kBN; r += 4)
-                            *reinterpret_cast<uint4 *>(dst + r * 128 + (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        fence_proxy_async_smem();
-                    }
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (vok) mbar_arrive_cluster(map_to_cta(smem_u32(v_tail), 0));
-                        else atomicExch(s_abort, 1);
-                    }
+            } else {
+                // The last V tile: land it against a local barrier, zero its
+                // rows past the last key, then tell the leader.
+                if (lane == 0) mbar_arrive_expect_tx(v_last, kVBytes);
+                __syncwarp();
+                if (PAGED) {
+                    if (lane < kBPT) tma_load_2d(dv + lane * BS * 128, &tm_v, v_last, c * 64, vrow);
+                } else if (lane == 0) {
+                    tma_load_3d(dv, &tm_v, v_last, c * 64, g, row0 + t * kBN);
+                }
+                const bool vok = __all_sync(0xffffffffu, mbar_wait(v_last, 0, a.err));
+                if (vok) {
+                    const int valid = kv_end_max - t * kBN;
+                    for (int r = valid + (lane >> 3); r < kBN; r += 4)
+                        *reinterpret_cast<uint4 *>(dv + r * 128 + (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (vok) mbar_arrive_cluster(map_to_cta(smem_u32(v_tail), 0));
+                    else atomicExch(s_abort, 1);
                 }
             }
             __syncwarp();
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // --------------------------------------------------------- MMA issue --
         if (c == 0 && lane == 0) {
+            const int k = warp - kMmaWarp;
+            const int nk = k == 0 ? nkt[0] : nkt[1];
+            const int nk_other = k == 0 ? nkt[1] : nkt[0];
             constexpr uint32_t kIdescS = umma_idesc_bf16(2 * kBM, kBN, false, false);
             constexpr uint32_t kIdescO = umma_idesc_bf16(2 * kBM, kD, false, true);
-            const uint64_t dq[2] = {umma_desc_sw128(smem_u32(smem + kQOff), 16, 1024),
-                                    umma_desc_sw128(smem_u32(smem + kQOff + kQBytes), 16, 1024)};
-            const uint64_t dp[2] = {umma_desc_sw128(smem_u32(smem + kPOff), 16, 1024),
-                                    umma_desc_sw128(smem_u32(smem + kPOff + kPBytes), 16, 1024)};
+            const uint64_t dq = umma_desc_sw128(smem_u32(smem + kQOff + k * kQBytes), 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(smem_u32(smem + kRingOff), 16, 1024);
             const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + kRingOff), kBox, 1024);
-            bool ok = mbar_wait_spin(q_full, 0, a.err);
-            auto issue_s = [&](int k, int t) {
-                const int i = 2 * t, sl = i % kSlots;
-                if (!ok) return;
-                const bool first = (k == 0) || nkt[0] <= t;
-                const bool last = (k == 1) || nkt[1] <= t;
-                if (first) {
-                    ok = mbar_wait_spin(&slot_full[sl], (i / kSlots) & 1, a.err);
-                    if (ok && t < T - 1)
-                        ok = mbar_wait_spin(&slot_full[(i + 1) % kSlots], ((i + 1) / kSlots) & 1, a.err);
-                    if (!ok) return;
-                }
-                tc_fence_after();
-                const uint64_t bk = dk0 + (uint64_t)((sl * kSlotBytes) >> 4);
-                const uint32_t d = tmem + k * kBN;
+            const uint32_t tS = tmem + k * kBN, tO = tmem + 2 * kBN + k * kD;
+            bool ok = nk == 0 || mbar_wait_spin(q_full, 0, a.err);
+            // S_k(t) = Q_k K(t)^T; the caller has waited for tile t.  The turn
+            // passes to the other thread four MMAs before the end, so that its
+            // wait overlaps MMAs still queued here.
+            auto issue_s = [&](int t) {
+                const uint64_t bk = dk0 + (uint64_t)(((t % kStages) * kStageBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    umma_bf16_pair(d, dq[k] + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    umma_bf16_pair(tS, dq + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
                                    bk + (uint64_t)(((kk >> 2) * kKHalf + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
-                umma_commit_pair(&s_full[k]);
-                if (last) umma_commit_pair(&slot_free[sl]);
-            };
-            auto issue_pv = [&](int k, int t) {
-                const int i = 2 * t + 1, sl = i % kSlots;
-                if (!ok || !(ok = mbar_wait_spin(&p_full[k], t & 1, a.err))) return;
-                const bool first = (k == 0) || nkt[0] <= t;
-                const bool last = (k == 1) || nkt[1] <= t;
-                if (t == T - 1 && first && !(ok = mbar_wait_spin(v_tail, 0, a.err))) return;
-                tc_fence_after();
-                const uint64_t bv = dv0 + (uint64_t)((sl * kSlotBytes) >> 4);
-                const uint32_t d = tmem + 2 * kBN + k * kD;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma_bf16_pair(d, dp[k] + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
-                                   bv + (uint64_t)((kk * 2048) >> 4), kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
-                if (t == nkt[k] - 1) umma_commit_pair(&o_done[k]);
-                if (last) umma_commit_pair(&slot_free[sl]);
-            };
-            if (nkt[0] > 0) issue_s(0, 0);
-            if (nkt[1] > 0) issue_s(1, 0);
-            for (int t = 0; t < T; ++t) {
-                if (t < nkt[0]) {
-                    issue_pv(0, t);
-                    if (t + 1 < nkt[0]) issue_s(0, t + 1);
+                    if (kk == 3) mbar_arrive(&turn[k]);
                 }
-                if (t < nkt[1]) {
-                    issue_pv(1, t);
-                    if (t + 1 < nkt[1]) issue_s(1, t + 1);
+            };
+            auto wait_tile = [&](int t) {
+                if (ok) ok = mbar_wait_spin(&tile_full[t % kStages], (t / kStages) & 1, a.err);
+            };
+            // The two threads take turns, group by group, in the order
+            //   S_0(0), S_1(0), [PV_0(0) S_0(1)], [PV_1(0) S_1(1)], [PV_0(1) S_0(2)], ...
+            // so that the tensor core works for one sub-tile while the other's
+            // softmax runs.  Group j of thread k is S_k(0) for j = 0 and
+            // [PV_k(j-1) S_k(j)] after; thread 1 waits for group j of thread
+            // 0, thread 0 for group j - 1 of thread 1 (each thread waits
+            // only while the other has MMAs queued).  Every wait comes before
+            // the turn is taken and every commit after the group's MMAs, so
+            // that a group goes out back to back.
+            auto other_group_exists = [&](int j) { return j == 0 ? nk_other > 0 : j - 1 < nk_other; };
+            auto take_turn = [&](int j) {  // before this thread's group j
+                const int jo = k == 0 ? j - 1 : j;
+                if (ok && jo >= 0 && other_group_exists(jo))
+                    ok = mbar_wait_spin(&turn[1 - k], jo & 1, a.err);
+            };
+            if (nk > 0) {
+                wait_tile(0);
+                take_turn(0);
+                if (ok) {
+                    issue_s(0);
+                    umma_commit_pair(&s_full[k]);
                 }
             }
+            for (int t = 0; t < nk && ok; ++t) {
+                // O_k += P_k(t) V(t), P_k from TMEM (written by the softmax warps)
+                const bool more = t + 1 < nk;
+                if (more) wait_tile(t + 1);
+                take_turn(t + 1);  // usually passed before P_k(t) is ready
+                if (!ok || !(ok = mbar_wait_spin(&p_full[k], t & 1, a.err))) break;
+                if (t == T - 1 && !(ok = mbar_wait_spin(v_tail, 0, a.err))) break;
+                tc_fence_after();
+                const uint64_t bv = dv0 + (uint64_t)(((t % kStages) * kStageBytes + kKBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    umma_bf16_pair_tmem_a(tO, tS + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
+                                          (t > 0 || kk > 0) ? 1u : 0u);
+                    if (kk == 3 && !more) mbar_arrive(&turn[k]);
+                }
+                if (more) issue_s(t + 1);  // overwrites P_k(t): after PV_k(t) in the tensor pipe
+                if (more) umma_commit_pair(&s_full[k]);
+                else umma_commit_pair(&o_done[k]);
+                umma_commit_pair(&tile_free[t % kStages]);
+                if (t >= nk_other) umma_commit_pair(&tile_free[t % kStages]);  // the only reader of tile t
+            }
+            // Do not let the pair tear down TMEM under MMAs still in flight.
+            umma_commit_pair(&mma_fin[k], 1);
+            mbar_wait(&mma_fin[k], 0, a.err);
             if (!ok) atomicExch(s_abort, 1);
         }
         __syncwarp();
     } else {
         // ----------------------------------------------------------- softmax --
-        // Warps 4k .. 4k+3 do sub-tile k; warp q owns rows 32q .. 32q+31 (TMEM
+        // Warps 2+4k .. 5+4k do sub-tile k; warp w owns rows 32q .. 32q+31 (TMEM
         // lane quadrant q), one row per thread, all 128 columns.
-        const int k = warp >> 2, q = warp & 3;
+        const int k = (warp - kSoftmaxWarp0) >> 2, q = warp & 3;
         const int r = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t tS = tmem + lane_base + k * kBN;
@@ -356,7 +377,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const RowTile my = k == 0 ? mine[0] : mine[1];
         const int nk = k == 0 ? nkt[0] : nkt[1];
         const uint32_t pf = map_to_cta(smem_u32(&p_full[k]), 0);
-        uint8_t *pbuf = smem + kPOff + k * kPBytes;
         const int lim_abs = min(p0 + my.q0 + r + 1, my.kv_end);
         const float sl = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
@@ -364,73 +384,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wait_warp = [&](uint64_t *bb, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait(bb, par, a.err));
         };
+        // One arrival per warp on the leader's barrier, after the warp's
+        // tcgen05 work is ordered before it.
+        auto arrive_leader = [&](uint64_t *bb, uint32_t remote) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (c == 0) mbar_arrive(bb);
+                else mbar_arrive_cluster(remote);
+            }
+        };
+        auto row_max = [&](const float *x) {
+            float m4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m4[i] = fmax3(x[i], x[i + 4], x[i + 8]);
+#pragma unroll
+            for (int j = 12; j < kBN; j += 8)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[j + i], j + 4 + i < kBN ? x[j + 4 + i] : -INFINITY);
+            return fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+        };
+        // P_k(t) = exp2(scale * S - mu) as bf16 pairs over the first 64 columns
+        // of S_k (column j: keys 2j, 2j+1); returns the row sum of the same
+        // rounded weights.  The TMEM stores are left in flight.
+        auto exps_to_tmem = [&](const float *x, float mu) {
+            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int cq = 0; cq < kBN / 32; ++cq) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    pk[j] = pack_bf16x2(fast_exp2(fmaf(x[32 * cq + 2 * j], sl, -mu)),
+                                        fast_exp2(fmaf(x[32 * cq + 2 * j + 1], sl, -mu)));
+                    ls2[j & 1] = add_f32x2(ls2[j & 1], bf16x2_unpack(pk[j]));
+                }
+                tmem_st16_async(tS + 16 * cq, pk);
+            }
+            return (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
+        };
         for (int t = 0; t < nk; ++t) {
+            // S_k(t) completing also means PV_k(t-1) has: O_k is stable and
+            // P_k(t-1) is no longer needed.
             if (!wait_warp(&s_full[k], t & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int lim = lim_abs - t * kBN;  // visible columns of this row
             float v[kBN];
             tmem_ld128(tS, v);
+            const int lim = lim_abs - t * kBN;  // visible columns of this row
             if (lim < kBN) {
 #pragma unroll
                 for (int j = 0; j < kBN; ++j)
                     if (j >= lim) v[j] = -INFINITY;
             }
-            float m4[4];
+            if (t == 0) {
+                // key 0 is visible to every row, so the maximum is finite
+                m_run = row_max(v) * sl;
+                l_run = exps_to_tmem(v, m_run);
+            } else {
+                // Exponentials against the running maximum; the row sum shows
+                // when the maximum has grown too far (weights above 2^64 or
+                // not finite): then move it, rescale O_k (stable: PV_k(t-1)
+                // has completed) and redo the tile.
+                float l_tile = exps_to_tmem(v, m_run);
+                if (__any_sync(0xffffffffu, !(l_tile <= 0x1p64f))) {
+                    const float m_new = fmaxf(m_run, row_max(v) * sl);
+                    const float alpha = fast_exp2(m_run - m_new);
+                    m_run = m_new;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) m4[i] = fmax3(v[i], v[i + 4], v[i + 8]);
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        float o[32];
+                        tmem_ld32(tO + cc * 32, o);
 #pragma unroll
-            for (int j = 12; j < kBN; j += 8)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], v[j + i], j + 4 + i < kBN ? v[j + 4 + i] : -INFINITY);
-            const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
-            const float m_new = fmaxf(m_run, mx * sl);
-            // Move the running maximum only when it grew by more than 2^8 for
-            // some row of the warp; O_k is rescaled after P is written.
-            const bool rescale = t > 0 && __any_sync(0xffffffffu, m_new > m_run + 8.f);
-            const float alpha = rescale ? fast_exp2(m_run - m_new) : 1.f;
-            if (t == 0 || rescale) m_run = m_new;
-            const float mu = m_run == -INFINITY ? 0.f : m_run;
-            // P_k(t) overwrites P_k(t-1): S_k(t) completing implies PV_k(t-1) read it.
-            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int jj = 0; jj < kBN / 8; ++jj) {
-                const uint4 pk = make_uint4(
-                    pack_bf16x2(fast_exp2(fmaf(v[jj * 8 + 0], sl, -mu)), fast_exp2(fmaf(v[jj * 8 + 1], sl, -mu))),
-                    pack_bf16x2(fast_exp2(fmaf(v[jj * 8 + 2], sl, -mu)), fast_exp2(fmaf(v[jj * 8 + 3], sl, -mu))),
-                    pack_bf16x2(fast_exp2(fmaf(v[jj * 8 + 4], sl, -mu)), fast_exp2(fmaf(v[jj * 8 + 5], sl, -mu))),
-                    pack_bf16x2(fast_exp2(fmaf(v[jj * 8 + 6], sl, -mu)), fast_exp2(fmaf(v[jj * 8 + 7], sl, -mu))));
-                // row sums of the same bf16-rounded weights that multiply V
-                ls2[0] = add_f32x2(ls2[0], bf16x2_unpack(pk.x));
-                ls2[1] = add_f32x2(ls2[1], bf16x2_unpack(pk.y));
-                ls2[0] = add_f32x2(ls2[0], bf16x2_unpack(pk.z));
-                ls2[1] = add_f32x2(ls2[1], bf16x2_unpack(pk.w));
-                *reinterpret_cast<uint4 *>(pbuf + (jj >> 3) * kBox + r * 128 + (((jj & 7) ^ (r & 7)) << 4)) = pk;
-            }
-            l_run = l_run * alpha + ((ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y));
-            if (rescale) {
-                // O_k is stable: S_k(t) completing implies PV_k(t-1) has, and
-                // PV_k(t) waits for this warp's arrival below.
-#pragma unroll
-                for (int cc = 0; cc < kD / 32; ++cc) {
-                    float o[32];
-                    tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(tO + cc * 32, o);
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(tO + cc * 32, o);
+                    }
+                    l_run *= alpha;
+                    l_tile = exps_to_tmem(v, m_run);
                 }
+                l_run += l_tile;
             }
-            // Every thread makes its P row visible to the tensor core, then one
-            // arrival per warp on the leader's barrier.
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (c == 0) mbar_arrive(&p_full[k]);
-                else mbar_arrive_cluster(pf);
-            }
+            tmem_wait_st();
+            arrive_leader(&p_full[k], pf);
         }
         // --------------------------------------------------------- epilogue --
         if (nk > 0) {

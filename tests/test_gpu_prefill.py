@@ -42,6 +42,34 @@ def test_prefill_dense_ragged(cuda_lib, Hq, Hkv, d):
     assert_close(out, ref, f"dense ragged Hq={Hq} Hkv={Hkv} d={d}")
 
 
+@pytest.mark.parametrize("slope", [1.0, 0.1, -0.1])
+def test_prefill_growing_scores(cuda_lib, slope):
+    """Scores that grow (or shrink) steadily along the keys: q . k_j ~ 8 slope j.
+    slope 1 moves every row's running maximum by ~2^130 per 128-key tile, 0.1 by
+    ~2^13 (a move past 2^64 every few tiles), -0.1 keeps the first key the
+    largest -- the paths where the kernel moves its running maximum and
+    rescales O."""
+    g = torch.Generator().manual_seed(23)
+    lens = [1000, 700, 129]
+    T, Hq, Hkv, d = sum(lens), 32, 8, 128
+    shape = wl.Shape(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=16, num_blocks=1)
+    q = (torch.randn(T, Hq, d, generator=g) * 0.1)
+    q[:, :, 0] = 8.0
+    k = (torch.randn(T, Hkv, d, generator=g) * 0.1)
+    pos = torch.cat([torch.arange(L, dtype=torch.float32) for L in lens])
+    k[:, :, 0] = slope * pos[:, None]
+    # Such peaked weights (about halving per key at slope 1) magnify the bf16
+    # rounding of P; V at half the usual spread keeps that within tolerance.
+    v = torch.randn(T, Hkv, d, generator=g) * 0.5
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    cu = np.zeros(len(lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    out = pa.prefill(shape, dev(q), dev(k), dev(v), dev(cu), max(lens))
+    pa.check_device_error()
+    ref = oracle.prefill(bits(q), bits(k), bits(v), cu)
+    assert_close(out, ref, f"growing scores slope={slope}")
+
+
 def _paged_case(seed, prefix_and_new, Hq, Hkv, d, B):
     """Sequences with `prefix` cached tokens (already in the pool) and `new`
     prompt rows; the new rows are appended on the GPU first."""
