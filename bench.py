@@ -409,7 +409,7 @@ def measure_prefill(pa, wl, dev, bf16_peak, peak_src, iters):
                      "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / bf16_peak, 4)}
         del kp, vp
     best = max(res.values(), key=lambda r: r["tflops"])
-    return {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, TMEM)", "unit": "TFLOP/s",
+    return {"bound": "tensor", "kernel": "prefill_pair_kernel (tcgen05 cta_group::2, P in TMEM; head_dim 128)", "unit": "TFLOP/s",
             "peak": bf16_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst)",
             "workloads": res, "achieved_best": best["tflops"], "frac_best": best["frac"],
             "flops_counted": "4*d*Hq per unmasked causal (row, key) pair", "l2": "flushed (256 MB write) before each launch"}
