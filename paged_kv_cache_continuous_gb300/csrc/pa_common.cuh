@@ -90,8 +90,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     }
 }
 
-// Wait by polling mbarrier.test_wait (never suspends): for a thread whose only
-// job is to react as soon as a phase completes, e.g. the MMA issuer.
+// Poll mbarrier.test_wait once (never suspends).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -104,12 +103,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Wait in mbarrier.try_wait without a time hint: the thread is suspended in
+// the barrier (issuing nothing) and resumes as soon as the phase completes --
+// for a thread whose only job is to react at once, e.g. an MMA issuer sharing
+// its SM sub-partition with busy warps.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, int *err) {
-    if (mbar_test_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if ((it & 1023u) == 0) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
             if (clock64() - t0 > kWaitLimitCycles) {
                 set_error(err, PA_ERR_TIMEOUT);
                 return false;

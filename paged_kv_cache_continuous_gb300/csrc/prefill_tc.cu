@@ -328,10 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tiles only) is applied once, in registers.
             float v[kBN];
             tmem_ld128(tS, v);
-            if (lim < kBN) {
+            // Warp-uniform branch: only tiles crossing some row's last key pay
+            // for the mask.
+            if (__any_sync(0xffffffffu, lim < kBN)) {
 #pragma unroll
-                for (int j = 0; j < kBN; ++j)
-                    if (j >= lim) v[j] = -INFINITY;
+                for (int j = 0; j < kBN; ++j) v[j] = j < lim ? v[j] : -INFINITY;
             }
             float m8[8];
 #pragma unroll

@@ -433,10 +433,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float v[kBN];
             tmem_ld128(tS, v);
             const int lim = lim_abs - t * kBN;  // visible columns of this row
-            if (lim < kBN) {
+            // Warp-uniform branch: only tiles crossing some row's last key pay
+            // for the mask.
+            if (__any_sync(0xffffffffu, lim < kBN)) {
 #pragma unroll
-                for (int j = 0; j < kBN; ++j)
-                    if (j >= lim) v[j] = -INFINITY;
+                for (int j = 0; j < kBN; ++j) v[j] = j < lim ? v[j] : -INFINITY;
             }
             if (t == 0) {
                 // key 0 is visible to every row, so the maximum is finite
