@@ -240,6 +240,7 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
     a.num_q_tiles = (max_q_len + 127) / 128;
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
+    a.num_sms = d->num_sms;
     cudaError_t e = sh->head_dim == 128 ? launch_prefill_pair(tq, tk, tv, a, sh->block_size, st)
                                         : launch_prefill(tq, tk, tv, a, sh->head_dim, sh->block_size, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -52,6 +52,7 @@ struct PrefillArgs {
     int max_q_len, num_q_tiles;
     int check_err_first;
     float scale_log2;
+    int num_sms;                 // persistent kernels size their grid from it
 };
 
 cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
