@@ -76,7 +76,11 @@ constexpr int kRingOff = 4 * kQBytes;
 constexpr int kStages = 3;                     // K/V ring
 constexpr int kBarOff = kRingOff + kStages * kStageBytes;
 constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 * 4 + 1 + 2 + 2;
-constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+constexpr int kSeqTableMax = 512;                     // sequences with a shared-memory tile count
+constexpr int kSeqInfoMax = 64;                       // ... and with their rows and prefix there too
+constexpr int kSeqTableOff = kBarOff + kNumBars * 8 + 16;
+constexpr int kSeqInfoOff = kSeqTableOff + kSeqTableMax * 2;
+constexpr int kSmemBytes = kSeqInfoOff + kSeqInfoMax * 12 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct RowTile {
@@ -112,22 +116,40 @@ constexpr int heads_per_pair(int mode) { return mode == 0 ? 4 : (mode == 1 ? 2 :
 
 // Unit v (longest causal rows first): false if it has no rows (or its
 // sequence's arguments are invalid, which is recorded in the error word).
+// A sequence's query rows, prefix and validity (bad arguments are recorded
+// in the error word; the sequence then has no work).
+template <bool PAGED, int BS>
+__device__ __forceinline__ bool seq_rows(const PrefillArgs &a, int s, int &row0, int &n, int &p0) {
+    row0 = a.cu_seqlens[s];
+    n = a.cu_seqlens[s + 1] - row0;
+    p0 = a.prefix_lens ? a.prefix_lens[s] : (a.seq_lens ? a.seq_lens[s] - n : 0);
+    const bool bad = n < 0 || p0 < 0 || row0 < 0 || (long long)row0 + n > a.num_tokens || n > a.max_q_len ||
+                     (PAGED && (p0 + n + BS - 1) / BS > a.max_blocks) || (!PAGED && p0 != 0);
+    if (bad) set_error(a.err, PA_ERR_BAD_INDEX);
+    return !bad;
+}
+
+// Unit v (longest causal rows first): false if it has no rows.  seq_tiles
+// holds each sequence's 128-row tile count (0 if invalid) for the first
+// kSeqTableMax sequences and seq_info their (row0, n, p0) for the first
+// kSeqInfoMax, so that looking a unit up costs no global load (which waits
+// behind the kernel's own TMA traffic).  Not inlined: every role runs the one
+// copy, which keeps it in the instruction cache between units.
 template <bool PAGED, int BS, int MODE>
-__device__ __forceinline__ bool unit_at(const PrefillArgs &a, int v, int c, Unit &u) {
+__device__ __noinline__ bool unit_at(const PrefillArgs &a, const uint16_t *seq_tiles, const int *seq_info, int v,
+                                     int c, Unit &u) {
     const int npx = (a.num_q_tiles + per_pair(MODE) - 1) / per_pair(MODE);
     const int ny = a.num_q_heads / heads_per_pair(MODE);
     const int px = npx - 1 - v / (ny * a.num_seqs);
     const int rem = v % (ny * a.num_seqs);
     const int y = rem % ny, s = rem / ny;
+    if (s < kSeqTableMax && px * per_pair(MODE) >= (int)seq_tiles[s]) return false;
     u.s = s;
-    u.row0 = a.cu_seqlens[s];
-    u.n = a.cu_seqlens[s + 1] - u.row0;
-    u.p0 = a.prefix_lens ? a.prefix_lens[s] : (a.seq_lens ? a.seq_lens[s] - u.n : 0);
-    const bool bad = u.n < 0 || u.p0 < 0 || u.row0 < 0 || (long long)u.row0 + u.n > a.num_tokens ||
-                     u.n > a.max_q_len || (PAGED && (u.p0 + u.n + BS - 1) / BS > a.max_blocks) ||
-                     (!PAGED && u.p0 != 0);
-    if (bad) {
-        set_error(a.err, PA_ERR_BAD_INDEX);
+    if (s < kSeqInfoMax) {
+        u.row0 = seq_info[3 * s];
+        u.n = seq_info[3 * s + 1];
+        u.p0 = seq_info[3 * s + 2];
+    } else if (!seq_rows<PAGED, BS>(a, s, u.row0, u.n, u.p0)) {
         return false;
     }
     RowTile rt[2][2];  // [cta][sub-tile]
@@ -174,6 +196,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bar + kNumBars);
     int *s_abort = reinterpret_cast<int *>(s_tmem + 1);
     volatile int *turn_cnt = reinterpret_cast<volatile int *>(s_abort + 1);  // [2] groups queued by thread k
+    uint16_t *seq_tiles = reinterpret_cast<uint16_t *>(smem + kSeqTableOff);
+    int *seq_info = reinterpret_cast<int *>(smem + kSeqInfoOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = (int)cluster_ctarank();
@@ -184,6 +208,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // alternating directions, which evens out the pairs' total work.
     auto unit_of = [&](int rnd) { return rnd * pairs + ((rnd & 1) ? pairs - 1 - pair : pair); };
 
+    for (int i = threadIdx.x; i < kSeqTableMax && i < a.num_seqs; i += kThreads) {
+        int row0, n, p0;
+        const bool good = seq_rows<PAGED, BS>(a, i, row0, n, p0);
+        seq_tiles[i] = good ? (uint16_t)((n + kBM - 1) / kBM) : 0;
+        if (i < kSeqInfoMax) {
+            seq_info[3 * i] = row0;
+            seq_info[3 * i + 1] = n;
+            seq_info[3 * i + 2] = p0;
+        }
+    }
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&q_full[b], 1);
@@ -236,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int v = unit_of(rnd);
             if (v >= num_units) continue;
             Unit u;
-            if (!unit_at<PAGED, BS, MODE>(a, v, c, u)) continue;
+            if (!unit_at<PAGED, BS, MODE>(a, seq_tiles, seq_info, v, c, u)) continue;
             const int qb = ord & 1;
             // Q buffer qb is free once both issuers' S MMAs of unit ord - 2 completed.
             if (lane == 0 && ord >= 2) ok = mbar_wait(&q_free[qb], ((ord >> 1) - 1) & 1, a.err);
@@ -373,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int v = unit_of(rnd);
             if (v >= num_units) continue;
                 Unit u;
-                if (!unit_at<PAGED, BS, MODE>(a, v, c, u)) continue;
+                if (!unit_at<PAGED, BS, MODE>(a, seq_tiles, seq_info, v, c, u)) continue;
                 const int qb = ord & 1;
                 const int nk = u.nkt[k], nk_other = u.nkt[1 - k];
                 const int groups[2] = {u.nkt[0] > 0 ? u.nkt[0] + 1 : 0, u.nkt[1] > 0 ? u.nkt[1] + 1 : 0};
@@ -514,7 +548,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int v = unit_of(rnd);
             if (v >= num_units) continue;
             Unit u;
-            if (!unit_at<PAGED, BS, MODE>(a, v, c, u)) continue;
+            if (!unit_at<PAGED, BS, MODE>(a, seq_tiles, seq_info, v, c, u)) continue;
             const int nk = u.nkt[k];
             if (nk == 0) continue;
             const RowTile &my = u.mine[k];
