@@ -244,6 +244,7 @@ def run_ours(args, world, rank, local):
 
     # ---- prefill half of the metric (tensor cores), timed alone with L2 flushed
     prefill = measure_prefill(pa, wl, dev, bf16_peak, peak_src, args.prefill_iters) if rank == 0 else None
+    copy = measure_copy(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
 
     clocks = clk.summary()
     traffic = load_traffic("decode_splitk", nbytes, st.num_seqs)
@@ -270,6 +271,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "prefill": prefill,
+        "block_copy": copy,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kp, vp, st, split, args.cpu_seconds)
@@ -413,6 +415,51 @@ def measure_prefill(pa, wl, dev, bf16_peak, peak_src, iters):
             "peak": bf16_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst)",
             "workloads": res, "achieved_best": best["tflops"], "frac_best": best["frac"],
             "flops_counted": "4*d*Hq per unmasked causal (row, key) pair", "l2": "flushed (256 MB write) before each launch"}
+
+
+def measure_copy(pa, wl, dev, hbm_peak, iters):
+    """Whole-block copies with the decode workload's block shape (32 KV heads x
+    16 tokens x 128 dims: 128 KB per block and pool): a 4096-block fork
+    inside a 1 GB device pool pair, and 1024-block swaps to and from pinned
+    host pools.  Bytes counted: K and V, read once and written once."""
+    shape = wl.Shape(num_q_heads=32, num_kv_heads=32, head_dim=128, block_size=16, num_blocks=8192)
+    blk = shape.num_kv_heads * shape.block_size * shape.head_dim * 2
+    kp = torch.empty((8192, 32, 16, 128), dtype=torch.bfloat16, device=dev).normal_()
+    vp = torch.empty_like(kp).normal_()
+    g = torch.Generator().manual_seed(17)
+    perm = torch.randperm(8192, generator=g).to(torch.int32)
+    src, dst = perm[:4096].to(dev), perm[4096:].to(dev)
+    hk = torch.empty((1024, 32, 16, 128), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    hids = torch.arange(1024, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(iters):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        pa.check_device_error()
+        return float(np.median([x.elapsed_time(y) for x, y in ts])) / 1e3
+
+    t_fork = timed(lambda: pa.copy_blocks(shape, kp, vp, kp, vp, src, dst))
+    t_out = timed(lambda: pa.copy_blocks(shape, kp, vp, hk, hv, src[:1024], hids))
+    t_in = timed(lambda: pa.copy_blocks(shape, hk, hv, kp, vp, hids, dst[:1024]))
+    fork_b, swap_b = 2 * 2 * 4096 * blk, 2 * 1024 * blk
+    return {"kernel": "copy_blocks_kernel", "block_bytes_per_pool": blk,
+            "fork_4096_blocks": {"ms": round(t_fork * 1e3, 4), "GBps": round(fork_b / t_fork / 1e9, 1),
+                                 "frac_hbm": round(fork_b / t_fork / 1e9 / hbm_peak, 4),
+                                 "bytes": "K+V read + written"},
+            "swap_out_1024_blocks": {"ms": round(t_out * 1e3, 4), "GBps": round(swap_b / t_out / 1e9, 1),
+                                     "bytes": "K+V moved to pinned host"},
+            "swap_in_1024_blocks": {"ms": round(t_in * 1e3, 4), "GBps": round(swap_b / t_in / 1e9, 1),
+                                    "bytes": "K+V moved from pinned host"}}
 
 
 # ------------------------------------------------------------ CPU oracle --

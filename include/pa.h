@@ -202,6 +202,30 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
                       int num_seqs, int max_seq_len, void *out, void *stream);
 
 /*
+ * Copy whole KV blocks between two pools of the same shape (num_kv_heads,
+ * block_size, head_dim; shape->num_blocks is not used here):
+ *     dst_k[dst_ids[i]] = src_k[src_ids[i]],  dst_v alike,  0 <= i < num_pairs
+ * (K and V, every KV head of the block).  The cache's GPU region and CPU region
+ * and the migration of a batch's cache between replicas (Blitzscale docs,
+ * sections "CacheManager" and "migration_queue") need this: within one pool it
+ * forks a sequence (copy-on-write), between device pools it migrates blocks,
+ * and with one side in pinned host memory (cudaHostAlloc, torch pin_memory) it
+ * swaps blocks out and back in -- the GPU reads or writes that memory through
+ * its device alias.  src_num_blocks / dst_num_blocks are the pools' sizes in
+ * blocks; an id outside them sets the device error word and that pair is
+ * skipped.  The id arrays are device memory.  A destination block must not
+ * also be a source, nor appear twice, in one call (the copies run in no fixed
+ * order).  Pools must be 16-byte aligned.  Returns PA_ERR_INVALID_ARG for a
+ * NULL, misaligned or pageable (not GPU-visible) pointer or a negative size,
+ * PA_ERR_UNSUPPORTED for a shape the library does not take; num_pairs == 0 is
+ * a no-op.  Asynchronous on `stream`; the caller owns every buffer.
+ */
+int pa_copy_blocks(const pa_shape_t *shape, const void *src_k, const void *src_v,
+                   int src_num_blocks, void *dst_k, void *dst_v, int dst_num_blocks,
+                   const int32_t *src_ids, const int32_t *dst_ids, int num_pairs,
+                   void *stream);
+
+/*
  * Validation mode (off by default, process-wide).  When on, each call first
  * runs a bounds-checking pass over block_table/slot_mapping/lengths; if it
  * finds a bad index it sets the device error word and the call's other

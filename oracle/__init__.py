@@ -138,6 +138,33 @@ def kv_append(k_new, v_new, slot_mapping, k_pool, v_pool, inplace: bool = False)
     return kp, vp
 
 
+def copy_blocks(src_k, src_v, dst_k, dst_v, src_ids, dst_ids):
+    """Whole-block copies between pools (Blitzscale docs, sections
+    "CacheManager" -- the cache's GPU and CPU regions -- and "migration_queue"):
+    return copies of (dst_k, dst_v) with dst[dst_ids[i]] = src[src_ids[i]].
+    Every copy reads the source as it was before the call.  Raises on an id
+    outside a pool, and -- when src and dst are the same pool -- on a
+    destination that is also a source.
+
+    Pools: uint16 [N, Hkv, B, d]; ids: int32 [n].
+    """
+    sk, sv = _u16(src_k), _u16(src_v)
+    dk, dv = _u16(dst_k).copy(), _u16(dst_v).copy()
+    si, di = _i32(src_ids), _i32(dst_ids)
+    if si.shape != di.shape:
+        raise ValueError("src_ids and dst_ids differ in length")
+    if sk.shape[1:] != dk.shape[1:]:
+        raise ValueError("pools differ in block shape")
+    if np.any((si < 0) | (si >= sk.shape[0])) or np.any((di < 0) | (di >= dk.shape[0])):
+        raise ValueError("copy_blocks: block id out of range")
+    if src_k is dst_k and np.intersect1d(si, di).size:
+        raise ValueError("copy_blocks: a destination block is also a source")
+    for s_, d_ in zip(si.tolist(), di.tolist()):
+        dk[d_] = sk[s_]
+        dv[d_] = sv[s_]
+    return dk, dv
+
+
 def expected_slots(q_start_loc, seq_lens, block_table, block_size) -> np.ndarray:
     qs, sl, bt = _i32(q_start_loc), _i32(seq_lens), _i32(block_table)
     S = sl.shape[0]

@@ -29,7 +29,7 @@ ERR_TIMEOUT = 7
 EXPORTS = [
     "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode",
     "pa_decode_noalloc", "pa_prefill",
-    "pa_mixed_step", "pa_set_validation", "pa_check_device_error", "pa_last_error",
+    "pa_mixed_step", "pa_copy_blocks", "pa_set_validation", "pa_check_device_error", "pa_last_error",
     "pa_set_decode_split",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
     "pa_alloc_num_free", "pa_alloc_num_blocks_of", "pa_alloc_block_table",
@@ -76,6 +76,7 @@ def load():
         "pa_decode_noalloc": ([SP, P, P, P, P, I, P, I, I, P, P], I),
         "pa_prefill": ([SP, P, P, P, P, P, P, I, I, I, I, P, P], I),
         "pa_mixed_step": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P], I),
+        "pa_copy_blocks": ([SP, P, P, I, P, P, I, P, P, I, P], I),
         "pa_set_validation": ([I], I),
         "pa_check_device_error": ([P], I),
         "pa_last_error": ([], ctypes.c_char_p),
@@ -162,6 +163,22 @@ def kv_append(shape, k_new, v_new, slot_mapping, k_pool, v_pool, stream=None):
     _check(load().pa_kv_append(ctypes.byref(_shape(shape)), _bf16(k_new, "k_new"), _bf16(v_new, "v_new"),
                                _i32(slot_mapping, "slot_mapping"), T, _bf16(k_pool, "k_pool"),
                                _bf16(v_pool, "v_pool"), _stream(stream)))
+
+
+def copy_blocks(shape, src_k, src_v, dst_k, dst_v, src_ids, dst_ids, stream=None):
+    """dst_k[dst_ids[i]] = src_k[src_ids[i]] (and V) for whole blocks.  Pools are
+    [N, Hkv, B, d] bf16 tensors on the GPU or in pinned host memory; the id
+    arrays are int32 on the GPU."""
+    for t, name in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v")):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    n = int(src_ids.shape[0])
+    if int(dst_ids.shape[0]) != n:
+        raise ValueError("src_ids and dst_ids differ in length")
+    _check(load().pa_copy_blocks(ctypes.byref(_shape(shape)), _bf16(src_k, "src_k"), _bf16(src_v, "src_v"),
+                                 int(src_k.shape[0]), _bf16(dst_k, "dst_k"), _bf16(dst_v, "dst_v"),
+                                 int(dst_k.shape[0]), _i32(src_ids, "src_ids"), _i32(dst_ids, "dst_ids"), n,
+                                 _stream(stream)))
 
 
 def decode(shape, q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, out=None,

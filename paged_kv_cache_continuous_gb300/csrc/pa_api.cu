@@ -366,6 +366,42 @@ int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new, 
     return ok();
 }
 
+int pa_copy_blocks(const pa_shape_t *shape, const void *src_k, const void *src_v, int src_num_blocks,
+                   void *dst_k, void *dst_v, int dst_num_blocks, const int32_t *src_ids,
+                   const int32_t *dst_ids, int num_pairs, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_pairs == 0) return ok();
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_ids || !dst_ids) return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+        return fail(PA_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    // Every pointer must be GPU-visible: device memory, or pinned host memory
+    // (read and written through its device alias).
+    const void *ptrs[6] = {src_k, src_v, dst_k, dst_v, src_ids, dst_ids};
+    void *dev_ptrs[6];
+    for (int i = 0; i < 6; ++i) {
+        cudaPointerAttributes at{};
+        cudaError_t pe = cudaPointerGetAttributes(&at, ptrs[i]);
+        if (pe != cudaSuccess) return cuda_fail(pe, "copy_blocks pointer query");
+        if (at.type == cudaMemoryTypeUnregistered || !at.devicePointer)
+            return fail(PA_ERR_INVALID_ARG, "copy_blocks: a pointer is neither device nor pinned host memory");
+        if (i >= 4 && at.type == cudaMemoryTypeHost)
+            return fail(PA_ERR_INVALID_ARG, "copy_blocks: block ids must be in device memory");
+        dev_ptrs[i] = at.devicePointer;
+    }
+    const long long block_bytes = (long long)shape->num_kv_heads * shape->block_size * shape->head_dim * 2;
+    cudaError_t e = launch_copy_blocks(dev_ptrs[0], dev_ptrs[1], dev_ptrs[2], dev_ptrs[3],
+                                       static_cast<const int32_t *>(dev_ptrs[4]),
+                                       static_cast<const int32_t *>(dev_ptrs[5]), num_pairs, block_bytes,
+                                       src_num_blocks, dst_num_blocks, d->num_sms, d->err, g_validation.load(),
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+    return ok();
+}
+
 int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
               const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
               int max_seq_len, void *out, void *workspace, size_t ws_bytes, void *stream) {

@@ -39,6 +39,12 @@ cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_
                              __nv_bfloat16 *v_pool, int *err, int check_err_first,
                              cudaStream_t stream);
 
+// Whole-block copies between pools (device or pinned host memory).
+cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                               const int32_t *src_ids, const int32_t *dst_ids, int num_pairs,
+                               long long block_bytes, int src_blocks, int dst_blocks, int num_sms, int *err,
+                               int check_err_first, cudaStream_t stream);
+
 // ------------------------------------------------------------ prefill ------
 struct PrefillArgs {
     const int32_t *cu_seqlens;   // [S+1] query rows of each sequence (in q/out)

@@ -312,11 +312,88 @@ def pin_mixed_step_composition():
         np.testing.assert_allclose(out[a:b], ref, rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------------------------------
+# Whole-block copies (fork, migration, swap)
+# ---------------------------------------------------------------------------
+
+def _fork_case():
+    """One 23-token sequence (B = 4: 6 blocks) in a 24-block pool; the 6
+    lowest free block ids receive the copies."""
+    shape = wl.Shape(num_q_heads=4, num_kv_heads=2, head_dim=16, block_size=4, num_blocks=24)
+    g = torch.Generator().manual_seed(31)
+    alloc = wl.BlockAllocator(shape.num_blocks, shape.block_size,
+                              torch.randperm(shape.num_blocks, generator=g).tolist())
+    st = wl.make_step(alloc, shape, [0], [23], [23], 0, g)
+    kp, vp = wl.new_pool(shape, 99)
+    kp, vp = oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, bits(kp), bits(vp))
+    src = st.block_table[0, :6].astype(np.int32)
+    dst = np.array([b for b in range(shape.num_blocks) if b not in set(src.tolist())][:6], dtype=np.int32)
+    q = wl.bf16_randn((1, 4, 16), g)
+    return shape, st, kp, vp, src, dst, q
+
+
+def pin_copy_blocks_fork_vs_sdpa():
+    """A sequence forked by copying its blocks inside the pool and pointing a
+    second table at the copies: decode over the fork equals SDPA over the
+    sequence's tokens in original order, the source blocks are untouched and
+    decode over the original table is unchanged."""
+    shape, st, kp, vp, src, dst, q = _fork_case()
+    kf, vf = oracle.copy_blocks(kp, vp, kp, vp, src, dst)
+    assert np.array_equal(kf[src], kp[src]) and np.array_equal(vf[src], vp[src])
+    bt2 = st.block_table.copy()
+    bt2[0, :6] = dst
+    lens = np.array([23], dtype=np.int32)
+    out_fork = oracle.decode(bits(q), kf, vf, bt2, lens)
+    ref = sdpa_rows(q, st.k_new, st.v_new)
+    np.testing.assert_allclose(out_fork, ref, rtol=0, atol=1e-12)
+    assert np.array_equal(out_fork, oracle.decode(bits(q), kf, vf, st.block_table, lens))
+
+
+def pin_copy_blocks_swap_round_trip():
+    """Swap out to a 10-block host pool and back into other device blocks: the
+    host pool holds token t of the sequence at [t // B][h][t % B] (the layout
+    written as numpy indexing), and decode through the swapped-in blocks equals
+    decode through the originals bit for bit."""
+    shape, st, kp, vp, src, dst, q = _fork_case()
+    zk = np.zeros((10,) + kp.shape[1:], dtype=np.uint16)
+    kh, vh = oracle.copy_blocks(kp, vp, zk, zk.copy(), src, np.arange(6, dtype=np.int32))
+    kn, vn = bits(st.k_new), bits(st.v_new)
+    for t in range(23):
+        assert np.array_equal(kh[t // 4, :, t % 4], kn[t]) and np.array_equal(vh[t // 4, :, t % 4], vn[t])
+    assert not kh[6:].any() and not vh[6:].any()
+    kd, vd = oracle.copy_blocks(kh, vh, kp, vp, np.arange(6, dtype=np.int32), dst)
+    bt2 = st.block_table.copy()
+    bt2[0, :6] = dst
+    lens = np.array([23], dtype=np.int32)
+    assert np.array_equal(oracle.decode(bits(q), kd, vd, bt2, lens),
+                          oracle.decode(bits(q), kp, vp, st.block_table, lens))
+
+
+def pin_copy_blocks_errors():
+    """Ids outside either pool and a destination that is also a source (same
+    pool) are rejected."""
+    shape, st, kp, vp, src, dst, q = _fork_case()
+    for bad_src, bad_dst in ((np.array([24], np.int32), np.array([0], np.int32)),
+                             (np.array([-1], np.int32), np.array([0], np.int32)),
+                             (np.array([0], np.int32), np.array([24], np.int32))):
+        try:
+            oracle.copy_blocks(kp, vp, kp.copy(), vp.copy(), bad_src, bad_dst)
+        except ValueError:
+            continue
+        raise AssertionError("out-of-range block id accepted")
+    try:
+        oracle.copy_blocks(kp, vp, kp, vp, src[:2], np.array([src[1], dst[0]], dtype=np.int32))
+    except ValueError:
+        return
+    raise AssertionError("overlapping source and destination accepted")
+
+
 ALL_PINS = [
     pin_decode_vs_sdpa, pin_prefill_dense_vs_sdpa, pin_prefill_paged_vs_sdpa,
     pin_chunked_prefill_vs_sdpa, pin_append_layout, pin_append_errors,
     pin_expected_slots_vs_allocator, pin_constant_v, pin_one_token_context,
     pin_zero_query_is_mean, pin_dominant_key, pin_two_key_golden,
     pin_block_permutation_invariance, pin_decode_equals_prefill_row,
-    pin_mixed_step_composition,
+    pin_mixed_step_composition, pin_copy_blocks_fork_vs_sdpa, pin_copy_blocks_swap_round_trip,
+    pin_copy_blocks_errors,
 ]

@@ -78,6 +78,25 @@ def test_null_and_misaligned_pointers(lib):
                              64, 8, DUMMY, DUMMY, DUMMY, DUMMY, 0, None) == binding.ERR_INVALID_ARG
 
 
+def test_copy_blocks_host_checks(lib):
+    sh = _shape()
+    odd = ctypes.c_void_p(0x1002)
+    # negative sizes, NULL and misaligned pools fail before any launch
+    assert lib.pa_copy_blocks(ctypes.byref(sh), DUMMY, DUMMY, 4, DUMMY, DUMMY, 4, DUMMY, DUMMY, -1,
+                              None) == binding.ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(ctypes.byref(sh), DUMMY, DUMMY, -4, DUMMY, DUMMY, 4, DUMMY, DUMMY, 1,
+                              None) == binding.ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(ctypes.byref(sh), DUMMY, None, 4, DUMMY, DUMMY, 4, DUMMY, DUMMY, 1,
+                              None) == binding.ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(ctypes.byref(sh), DUMMY, DUMMY, 4, odd, DUMMY, 4, DUMMY, DUMMY, 1,
+                              None) == binding.ERR_INVALID_ARG
+    bad = _shape(head_dim=96)
+    assert lib.pa_copy_blocks(ctypes.byref(bad), DUMMY, DUMMY, 4, DUMMY, DUMMY, 4, DUMMY, DUMMY, 1,
+                              None) == binding.ERR_UNSUPPORTED
+    # nothing to copy: a no-op even with NULL pointers
+    assert lib.pa_copy_blocks(ctypes.byref(sh), None, None, 0, None, None, 0, None, None, 0, None) == binding.OK
+
+
 def test_empty_calls_are_noops(lib):
     sh = _shape()
     assert lib.pa_kv_append(ctypes.byref(sh), None, None, None, 0, None, None, None) == binding.OK

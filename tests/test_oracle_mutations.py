@@ -5,6 +5,7 @@ import subprocess
 import tempfile
 from pathlib import Path
 
+import numpy as np
 import pytest
 
 import oracle
@@ -57,3 +58,48 @@ def test_mutant_is_caught(name, orig, repl, count, monkeypatch):
             except (AssertionError, oracle.OracleError):
                 caught.append(pin.__name__)
         assert caught, f"mutation {name} passed every pin"
+
+
+# Python-level mistakes in the block copy (it is plain numpy, not C).
+_copy = oracle.copy_blocks
+
+
+def _copy_k_only(sk, sv, dk, dv, si, di):
+    dk2, _ = _copy(sk, sv, dk, dv, si, di)
+    return dk2, np.array(dv, dtype=np.uint16, copy=True)
+
+
+def _ids_swapped(sk, sv, dk, dv, si, di):
+    if sk is dk:
+        dk, dv = np.array(dk, copy=True), np.array(dv, copy=True)
+    return _copy(sk, sv, dk, dv, di, si)
+
+
+def _next_block(sk, sv, dk, dv, si, di):
+    n = np.asarray(dk).shape[0]
+    return _copy(sk, sv, dk, dv, si, ((np.asarray(di, dtype=np.int64) + 1) % n).astype(np.int32))
+
+
+def _no_checks(sk, sv, dk, dv, si, di):
+    sk, sv = np.asarray(sk), np.asarray(sv)
+    dk2, dv2 = np.array(dk, copy=True), np.array(dv, copy=True)
+    for s_, d_ in zip(np.asarray(si).tolist(), np.asarray(di).tolist()):
+        dk2[d_ % dk2.shape[0]] = sk[s_ % sk.shape[0]]
+        dv2[d_ % dv2.shape[0]] = sv[s_ % sv.shape[0]]
+    return dk2, dv2
+
+
+COPY_MUTANTS = [("copy_k_only", _copy_k_only), ("ids_swapped", _ids_swapped),
+                ("next_block", _next_block), ("no_checks", _no_checks)]
+
+
+@pytest.mark.parametrize("name,fn", COPY_MUTANTS, ids=[m[0] for m in COPY_MUTANTS])
+def test_copy_mutant_is_caught(name, fn, monkeypatch):
+    monkeypatch.setattr(oracle, "copy_blocks", fn)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, oracle.OracleError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"mutation {name} passed every pin"
