@@ -76,12 +76,21 @@ constexpr int kRingOff = 4 * kQBytes;
 constexpr int kStages = 3;                     // K/V ring
 constexpr int kBarOff = kRingOff + kStages * kStageBytes;
 constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 * 4 + 1 + 2 + 2;
-constexpr int kSeqTableMax = 512;                     // sequences with a shared-memory tile count
-constexpr int kSeqInfoMax = 64;                       // ... and with their rows and prefix there too
-constexpr int kSeqTableOff = kBarOff + kNumBars * 8 + 16;
-constexpr int kSeqInfoOff = kSeqTableOff + kSeqTableMax * 2;
-constexpr int kSmemBytes = kSeqInfoOff + kSeqInfoMax * 12 + 1024;
+// The schedule: with at most kSeqMax sequences and kMaxLevels row-tile levels
+// the units are dealt from a list in shared memory that holds non-empty units
+// only; otherwise every (level, head group, sequence) slot is dealt and empty
+// ones are skipped.
+constexpr int kSeqMax = 512;                             // sequences in the shared-memory schedule
+constexpr int kSeqInfoMax = 64;                          // ... with (row0, n, p0) cached there too
+constexpr int kMaxLevels = 64;                           // row-tile levels (units per head and sequence)
+constexpr int kSeqKeyOff = kBarOff + kNumBars * 8 + 16;  // uint8 [kSeqMax]: a sequence's levels
+constexpr int kSeqOrderOff = kSeqKeyOff + kSeqMax;       // uint16 [kSeqMax]: sequences, most levels first
+constexpr int kSeqInfoOff = kSeqOrderOff + kSeqMax * 2;  // int [kSeqInfoMax][3]: row0, n, p0
+constexpr int kLevelOff = kSeqInfoOff + kSeqInfoMax * 12;   // int [kMaxLevels + 1]: units above a level
+constexpr int kCountOff = kLevelOff + (kMaxLevels + 1) * 4; // int [kMaxLevels + 1]: scratch counts
+constexpr int kSmemBytes = kCountOff + (kMaxLevels + 1) * 4;
 static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kSeqInfoOff % 4 == 0, "alignment");
 
 struct RowTile {
     int h, q0, rows, kv_end;
@@ -105,11 +114,19 @@ __device__ __forceinline__ void row_tile(RowTile &rt, int c, int k, int px, int 
     rt.kv_end = p0 + min(n, rt.q0 + kBM);
 }
 
-// One work unit, identical in both CTAs and all roles.
+// One work unit, identical in both CTAs and all roles (scalars only, so that
+// it lives in registers).
 struct Unit {
-    int s, row0, n, p0, g, T, kv_end_max, nkt[2];
-    RowTile mine[2];  // this CTA's two sub-tiles
+    int s, px, y, row0, n, p0, g, T, kv_end_max, nkt0, nkt1;
 };
+
+// This CTA's sub-tile k of unit u.
+template <int MODE>
+__device__ __forceinline__ RowTile my_tile(const Unit &u, int c, int k) {
+    RowTile rt;
+    row_tile<MODE>(rt, c, k, u.px, u.y, u.n, u.p0);
+    return rt;
+}
 
 constexpr int per_pair(int mode) { return mode == 0 ? 1 : (mode == 1 ? 2 : 4); }   // row tiles per head
 constexpr int heads_per_pair(int mode) { return mode == 0 ? 4 : (mode == 1 ? 2 : 1); }
@@ -129,48 +146,56 @@ __device__ __forceinline__ bool seq_rows(const PrefillArgs &a, int s, int &row0,
     return !bad;
 }
 
-// Unit v (longest causal rows first): false if it has no rows.  seq_tiles
-// holds each sequence's 128-row tile count (0 if invalid) for the first
-// kSeqTableMax sequences and seq_info their (row0, n, p0) for the first
-// kSeqInfoMax, so that looking a unit up costs no global load (which waits
-// behind the kernel's own TMA traffic).  Not inlined: every role runs the one
-// copy, which keeps it in the instruction cache between units.
+// The unit dealt as number v (longest causal rows first): false if it has no
+// rows.  In the compact schedule, level lvl (row tile px = npx - 1 - lvl) holds
+// ny units for each sequence with more than px levels, in the order of
+// seq_order; `lvl` is the caller's cursor (v only grows).  Otherwise v walks
+// every (level, sequence, head group) slot.  A sequence's (row0, n, p0) comes
+// from shared memory for the first kSeqInfoMax sequences.
 template <bool PAGED, int BS, int MODE>
-__device__ __noinline__ bool unit_at(const PrefillArgs &a, const uint16_t *seq_tiles, const int *seq_info, int v,
-                                     int c, Unit &u) {
-    const int npx = (a.num_q_tiles + per_pair(MODE) - 1) / per_pair(MODE);
-    const int ny = a.num_q_heads / heads_per_pair(MODE);
-    const int px = npx - 1 - v / (ny * a.num_seqs);
-    const int rem = v % (ny * a.num_seqs);
-    const int y = rem % ny, s = rem / ny;
-    if (s < kSeqTableMax && px * per_pair(MODE) >= (int)seq_tiles[s]) return false;
-    u.s = s;
-    if (s < kSeqInfoMax) {
-        u.row0 = seq_info[3 * s];
-        u.n = seq_info[3 * s + 1];
-        u.p0 = seq_info[3 * s + 2];
-    } else if (!seq_rows<PAGED, BS>(a, s, u.row0, u.n, u.p0)) {
+__device__ __forceinline__ bool unit_at(const PrefillArgs &a, const uint8_t *smem, bool compact, int npx, int ny,
+                                        int v, int &lvl, Unit &u) {
+    const int *lcum = reinterpret_cast<const int *>(smem + kLevelOff);
+    const int *seq_info = reinterpret_cast<const int *>(smem + kSeqInfoOff);
+    if (compact) {
+        while (lvl < npx && v >= lcum[lvl + 1]) ++lvl;
+        if (lvl >= npx) return false;
+        const int r = v - lcum[lvl];
+        u.px = npx - 1 - lvl;
+        u.y = r % ny;
+        u.s = reinterpret_cast<const uint16_t *>(smem + kSeqOrderOff)[r / ny];
+    } else {
+        u.px = npx - 1 - v / (ny * a.num_seqs);
+        const int rem = v % (ny * a.num_seqs);
+        u.y = rem % ny;
+        u.s = rem / ny;
+    }
+    if (u.s < kSeqInfoMax) {
+        u.row0 = seq_info[3 * u.s];
+        u.n = seq_info[3 * u.s + 1];
+        u.p0 = seq_info[3 * u.s + 2];
+    } else if (!seq_rows<PAGED, BS>(a, u.s, u.row0, u.n, u.p0)) {
         return false;
     }
+    if (u.px * per_pair(MODE) * kBM >= u.n) return false;
     RowTile rt[2][2];  // [cta][sub-tile]
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-        for (int k = 0; k < 2; ++k) row_tile<MODE>(rt[cc][k], cc, k, px, y, u.n, u.p0);
-    u.kv_end_max = 0;
+        for (int k = 0; k < 2; ++k) row_tile<MODE>(rt[cc][k], cc, k, u.px, u.y, u.n, u.p0);
+    int e[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        int e = 0;
+        e[k] = 0;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
-            if (rt[cc][k].rows > 0) e = max(e, rt[cc][k].kv_end);
-        u.nkt[k] = (e + kBN - 1) / kBN;
-        u.kv_end_max = max(u.kv_end_max, e);
+            if (rt[cc][k].rows > 0) e[k] = max(e[k], rt[cc][k].kv_end);
     }
-    u.T = max(u.nkt[0], u.nkt[1]);
+    u.nkt0 = (e[0] + kBN - 1) / kBN;
+    u.nkt1 = (e[1] + kBN - 1) / kBN;
+    u.kv_end_max = max(e[0], e[1]);
+    u.T = max(u.nkt0, u.nkt1);
     u.g = rt[0][0].h / a.group;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) row_tile<MODE>(u.mine[k], c, k, px, y, u.n, u.p0);
     return u.T > 0;
 }
 
@@ -178,9 +203,10 @@ template <int BS, bool PAGED, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // Dynamic shared memory starts 1024-byte aligned (checked below: the
+    // swizzled TMA/MMA buffers need it).
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *q_full = bar;                     // [2] leader: a unit's Q landed in both CTAs (Q buffer b)
     uint64_t *q_free = q_full + 2;              // [2] both issuers' S MMAs of the unit in Q buffer b completed
@@ -196,26 +222,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bar + kNumBars);
     int *s_abort = reinterpret_cast<int *>(s_tmem + 1);
     volatile int *turn_cnt = reinterpret_cast<volatile int *>(s_abort + 1);  // [2] groups queued by thread k
-    uint16_t *seq_tiles = reinterpret_cast<uint16_t *>(smem + kSeqTableOff);
+    uint8_t *seq_key = smem + kSeqKeyOff;
+    uint16_t *seq_order = reinterpret_cast<uint16_t *>(smem + kSeqOrderOff);
     int *seq_info = reinterpret_cast<int *>(smem + kSeqInfoOff);
+    int *lcum = reinterpret_cast<int *>(smem + kLevelOff);
+    int *cnt = reinterpret_cast<int *>(smem + kCountOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = (int)cluster_ctarank();
     const int pairs = (int)(gridDim.x >> 1), pair = (int)(blockIdx.x >> 1);
-    const int num_units = ((a.num_q_tiles + per_pair(MODE) - 1) / per_pair(MODE)) *
-                          (a.num_q_heads / heads_per_pair(MODE)) * a.num_seqs;
+    const int npx = (a.num_q_tiles + per_pair(MODE) - 1) / per_pair(MODE);  // levels
+    const int ny = a.num_q_heads / heads_per_pair(MODE);                       // head groups
+    const bool compact = a.num_seqs <= kSeqMax && npx <= kMaxLevels;
     // Units are numbered longest first; round rnd deals them to the pairs in
     // alternating directions, which evens out the pairs' total work.
     auto unit_of = [&](int rnd) { return rnd * pairs + ((rnd & 1) ? pairs - 1 - pair : pair); };
 
-    for (int i = threadIdx.x; i < kSeqTableMax && i < a.num_seqs; i += kThreads) {
+    // The schedule (identical in both CTAs): each sequence's level count
+    // (key), the number of sequences above each level, and the sequences
+    // ordered by key, most first (stable, so both CTAs agree).
+    if (compact)
+        for (int j = threadIdx.x; j <= npx; j += kThreads) cnt[j] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.num_seqs && (compact || i < kSeqInfoMax); i += kThreads) {
         int row0, n, p0;
         const bool good = seq_rows<PAGED, BS>(a, i, row0, n, p0);
-        seq_tiles[i] = good ? (uint16_t)((n + kBM - 1) / kBM) : 0;
         if (i < kSeqInfoMax) {
             seq_info[3 * i] = row0;
-            seq_info[3 * i + 1] = n;
+            seq_info[3 * i + 1] = good ? n : 0;
             seq_info[3 * i + 2] = p0;
+        }
+        if (compact) {
+            const int key = good ? ((n + kBM - 1) / kBM + per_pair(MODE) - 1) / per_pair(MODE) : 0;
+            seq_key[i] = (uint8_t)key;
+            atomicAdd(&cnt[key], 1);
+        }
+    }
+    __syncthreads();
+    if (compact && warp == kSoftmaxWarp0) {
+        if (lane == 0) {
+            // cnt[j] becomes the number of sequences with more than j levels
+            // (= the first slot of key j in the descending order)
+            int acc = 0;
+            for (int j = npx; j >= 0; --j) {
+                const int h = cnt[j];
+                cnt[j] = acc;
+                acc += h;
+            }
+            int cum = 0;
+            lcum[0] = 0;
+            for (int l = 0; l < npx; ++l) {
+                cum += ny * cnt[npx - 1 - l];
+                lcum[l + 1] = cum;
+            }
+        }
+        __syncwarp();
+        for (int b0 = 0; b0 < a.num_seqs; b0 += 32) {
+            const int i = b0 + lane;
+            const int key = i < a.num_seqs ? (int)seq_key[i] : -1;
+            const unsigned grp = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(grp & ((1u << lane) - 1u));
+            if (key > 0) seq_order[cnt[key] + rank] = (uint16_t)i;
+            __syncwarp();
+            if (key > 0 && rank == 0) cnt[key] += __popc(grp);
+            __syncwarp();
         }
     }
     if (threadIdx.x == 0) {
@@ -239,6 +309,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Validation mode: the leader's reading of the error word decides for
         // both CTAs (it may change while the kernel runs).
         *s_abort = (a.check_err_first && *(volatile int *)a.err != 0) ? 1 : 0;
+        if (smem_u32(smem) & 1023u) {  // never seen; refuse rather than compute garbage
+            set_error(a.err, PA_ERR_UNSUPPORTED);
+            *s_abort = 1;
+        }
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -251,6 +325,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const bool skip = ld_shared_cluster(map_to_cta(smem_u32(s_abort), 0)) != 0;
+    const int num_units = compact ? lcum[npx] : npx * ny * a.num_seqs;
 
     if (skip) {
         // nothing to do: fall through to the pair-wide teardown
@@ -264,13 +339,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
-        int ord = 0, gb = 0;  // units done, global index of the unit's first tile
+        int ord = 0, gb = 0, lvl = 0;  // units done, global index of the unit's first tile, schedule cursor
         bool ok = true;
         for (int rnd = 0; rnd * pairs < num_units && ok; ++rnd) {
             const int v = unit_of(rnd);
             if (v >= num_units) continue;
             Unit u;
-            if (!unit_at<PAGED, BS, MODE>(a, seq_tiles, seq_info, v, c, u)) continue;
+            if (!unit_at<PAGED, BS, MODE>(a, smem, compact, npx, ny, v, lvl, u)) continue;
             const int qb = ord & 1;
             // Q buffer qb is free once both issuers' S MMAs of unit ord - 2 completed.
             if (lane == 0 && ord >= 2) ok = mbar_wait(&q_free[qb], ((ord >> 1) - 1) & 1, a.err);
@@ -280,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && c == 0) mbar_arrive_expect_tx(&q_full[qb], 2 * 2 * kQBytes);
             __syncwarp();
             if (lane < 4) {  // lane = 2 sub-tile + half
-                const RowTile &rt = (lane >> 1) ? u.mine[1] : u.mine[0];
+                const RowTile rt = my_tile<MODE>(u, c, lane >> 1);
                 tma_load_3d_pair(smem + kQOff + (2 * qb + (lane >> 1)) * kQBytes + (lane & 1) * kBox, &tm_q, lq,
                                  (lane & 1) * 64, rt.h, u.row0 + rt.q0);
             }
@@ -379,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t dv0 = umma_desc_sw128(smem_u32(smem + kRingOff + kKBytes), kBox, 1024);
             const uint32_t tS = tmem + k * kBN, tO = tmem + 2 * kBN + k * kD;
             bool ok = true;
-            int ord = 0, gb = 0;       // units done, global index of the unit's first tile
+            int ord = 0, gb = 0, lvl = 0;  // units done, first tile of the unit, schedule cursor
             int pc = 0, uo = 0;        // P_k(t) phases seen, units of sub-tile k done
             int gbase[2] = {0, 0};     // groups issued by each thread before this unit
             int mine_q = 0;            // groups this thread has queued
@@ -407,10 +482,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int v = unit_of(rnd);
             if (v >= num_units) continue;
                 Unit u;
-                if (!unit_at<PAGED, BS, MODE>(a, seq_tiles, seq_info, v, c, u)) continue;
+                if (!unit_at<PAGED, BS, MODE>(a, smem, compact, npx, ny, v, lvl, u)) continue;
                 const int qb = ord & 1;
-                const int nk = u.nkt[k], nk_other = u.nkt[1 - k];
-                const int groups[2] = {u.nkt[0] > 0 ? u.nkt[0] + 1 : 0, u.nkt[1] > 0 ? u.nkt[1] + 1 : 0};
+                const int nk = k ? u.nkt1 : u.nkt0, nk_other = k ? u.nkt0 : u.nkt1;
+                const int groups[2] = {u.nkt0 > 0 ? u.nkt0 + 1 : 0, u.nkt1 > 0 ? u.nkt1 + 1 : 0};
                 // The two threads take turns, group by group, in the order
                 //   S_0(0), S_1(0), [PV_0(0) S_0(1)], [PV_1(0) S_1(1)], ...
                 // so that the tensor core works for one sub-tile while the
@@ -502,7 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t of = map_to_cta(smem_u32(&o_free[k]), 0);
         const float sl = a.scale_log2;
         bool ok = true;
-        int sc = 0, uo = 0;  // S_k phases seen, units of sub-tile k done
+        int sc = 0, uo = 0, lvl = 0;  // S_k phases seen, units of sub-tile k done, schedule cursor
         auto wait_warp = [&](uint64_t *bb, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait(bb, par, a.err));
         };
@@ -548,10 +623,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int v = unit_of(rnd);
             if (v >= num_units) continue;
             Unit u;
-            if (!unit_at<PAGED, BS, MODE>(a, seq_tiles, seq_info, v, c, u)) continue;
-            const int nk = u.nkt[k];
+            if (!unit_at<PAGED, BS, MODE>(a, smem, compact, npx, ny, v, lvl, u)) continue;
+            const int nk = k ? u.nkt1 : u.nkt0;
             if (nk == 0) continue;
-            const RowTile &my = u.mine[k];
+            const RowTile my = my_tile<MODE>(u, c, k);
             const int lim_abs = min(u.p0 + my.q0 + r + 1, my.kv_end);  // keys visible to row r
             float m_run = 0.f, l_run = 0.f;
             for (int t = 0; t < nk; ++t) {
@@ -572,33 +647,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < kBN; ++j) v[j] = j < lim ? v[j] : -INFINITY;
                 }
-                if (t == 0) {
-                    // key 0 is visible to every row, so the maximum is finite
-                    m_run = row_max(v) * sl;
-                    l_run = exps_to_tmem(v, m_run);
-                } else {
-                    // Exponentials against the running maximum; the row sum shows
-                    // when the maximum has grown too far (weights above 2^64 or
-                    // not finite): then move it, rescale O_k (stable: PV_k(t-1)
-                    // has completed) and redo the tile.
-                    float l_tile = exps_to_tmem(v, m_run);
-                    if (__any_sync(0xffffffffu, !(l_tile <= 0x1p64f))) {
-                        const float m_new = fmaxf(m_run, row_max(v) * sl);
-                        const float alpha = fast_exp2(m_run - m_new);
-                        m_run = m_new;
+                // key 0 is visible to every row, so the first tile's maximum is finite
+                if (t == 0) m_run = row_max(v) * sl;
+                // Exponentials against the running maximum (one copy of the code
+                // for every tile, which keeps it in the instruction cache); the row
+                // sum shows when the maximum has grown too far (weights above 2^64
+                // or not finite): then move it, rescale O_k (stable: PV_k(t-1) has
+                // completed) and redo the tile, once.  Never taken for t == 0.
+                float l_tile;
+#pragma unroll 1
+                for (int pass = 0;; ++pass) {
+                    l_tile = exps_to_tmem(v, m_run);
+                    if (pass > 0 || t == 0 || !__any_sync(0xffffffffu, !(l_tile <= 0x1p64f))) break;
+                    const float m_new = fmaxf(m_run, row_max(v) * sl);
+                    const float alpha = fast_exp2(m_run - m_new);
+                    m_run = m_new;
 #pragma unroll
-                        for (int cc = 0; cc < kD / 32; ++cc) {
-                            float o[32];
-                            tmem_ld32(tO + cc * 32, o);
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        float o[32];
+                        tmem_ld32(tO + cc * 32, o);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                            tmem_st32(tO + cc * 32, o);
-                        }
-                        l_run *= alpha;
-                        l_tile = exps_to_tmem(v, m_run);
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(tO + cc * 32, o);
                     }
-                    l_run += l_tile;
+                    l_run *= alpha;
                 }
+                l_run = (t == 0) ? l_tile : l_run + l_tile;
                 tmem_wait_st();
                 arrive_leader(&p_full[k], pf);
             }
