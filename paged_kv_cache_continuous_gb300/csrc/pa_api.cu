@@ -241,8 +241,14 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
     a.num_sms = d->num_sms;
-    cudaError_t e = sh->head_dim == 128 ? launch_prefill_pair(tq, tk, tv, a, sh->block_size, st)
-                                        : launch_prefill(tq, tk, tv, a, sh->head_dim, sh->block_size, st);
+    cudaError_t e;
+    if (sh->head_dim == 128) {
+        CUtensorMap to;
+        if ((rc = make_rows_map(&to, out, sh->head_dim, sh->num_q_heads, num_tokens, 32))) return rc;
+        e = launch_prefill_pair(tq, tk, tv, to, a, sh->block_size, st);
+    } else {
+        e = launch_prefill(tq, tk, tv, a, sh->head_dim, sh->block_size, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PA_OK;
 }

@@ -67,8 +67,9 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
 
 // head_dim 128 on CTA pairs (M = 256 tcgen05.mma).  Dense form: tm_k boxes
 // are 64 rows (each CTA of the pair loads half of a 128-key tile).
+// tm_o: out as rows [T][Hq][d], boxes of 64 columns x 1 head x 32 rows.
 cudaError_t launch_prefill_pair(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                const CUtensorMap &tm_v, const PrefillArgs &a,
+                                const CUtensorMap &tm_v, const CUtensorMap &tm_o, const PrefillArgs &a,
                                 int block_size, cudaStream_t stream);
 
 // --------------------------------------------------------- validation ------

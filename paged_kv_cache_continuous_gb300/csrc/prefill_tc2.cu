@@ -202,14 +202,16 @@ __device__ __forceinline__ bool unit_at(const PrefillArgs &a, const uint8_t *sme
 template <int BS, bool PAGED, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const PrefillArgs a) {
     // Dynamic shared memory starts 1024-byte aligned (checked below: the
     // swizzled TMA/MMA buffers need it).
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *q_full = bar;                     // [2] leader: a unit's Q landed in both CTAs (Q buffer b)
-    uint64_t *q_free = q_full + 2;              // [2] both issuers' S MMAs of the unit in Q buffer b completed
+    uint64_t *q_free = q_full + 2;              // [2] local: Q buffer b is free -- both issuers' S MMAs of its
+                                                //     unit completed and the 8 softmax warps' output staging in it is read
     uint64_t *tile_full = q_free + 2;           // [kStages] leader: K and V of a tile landed in both CTAs
     uint64_t *tile_free = tile_full + kStages;  // [kStages] both sub-tiles' MMAs on the tile have completed
     uint64_t *s_full = tile_free + kStages;     // [2] S_k(t) is in TMEM (commit, both CTAs)
@@ -291,7 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&q_full[b], 1);
-            mbar_init(&q_free[b], 2);  // one commit per issuing thread
+            mbar_init(&q_free[b], 2 + 8);  // one commit per issuing thread, one arrival per softmax warp
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 2 * 4);  // one arrival per softmax warp of each CTA
             mbar_init(&o_done[b], 1);
@@ -347,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             Unit u;
             if (!unit_at<PAGED, BS, MODE>(a, smem, compact, npx, ny, v, lvl, u)) continue;
             const int qb = ord & 1;
-            // Q buffer qb is free once both issuers' S MMAs of unit ord - 2 completed.
+            // Q buffer qb is free once unit ord - 2 is done with it (S MMAs, output staging).
             if (lane == 0 && ord >= 2) ok = mbar_wait(&q_free[qb], ((ord >> 1) - 1) & 1, a.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok || *(volatile int *)s_abort) break;
@@ -577,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t of = map_to_cta(smem_u32(&o_free[k]), 0);
         const float sl = a.scale_log2;
         bool ok = true;
-        int sc = 0, uo = 0, lvl = 0;  // S_k phases seen, units of sub-tile k done, schedule cursor
+        int sc = 0, uo = 0, lvl = 0, ord = 0;  // S_k phases seen, units of sub-tile k done, schedule cursor, units
         auto wait_warp = [&](uint64_t *bb, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait(bb, par, a.err));
         };
@@ -625,7 +627,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             Unit u;
             if (!unit_at<PAGED, BS, MODE>(a, smem, compact, npx, ny, v, lvl, u)) continue;
             const int nk = k ? u.nkt1 : u.nkt0;
-            if (nk == 0) continue;
+            const int qb = ord & 1;
+            ++ord;
+            if (nk == 0) {  // nothing of this sub-tile in the unit: its Q buffer half is not staged
+                if (lane == 0) mbar_arrive(&q_free[qb]);
+                continue;
+            }
             const RowTile my = my_tile<MODE>(u, c, k);
             const int lim_abs = min(u.p0 + my.q0 + r + 1, my.kv_end);  // keys visible to row r
             float m_run = 0.f, l_run = 0.f;
@@ -689,18 +696,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld128(tO, o);
             arrive_leader(&o_free[k], of);
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            if (r < my.rows) {
-                __nv_bfloat16 *orow = a.out + ((size_t)(u.row0 + my.q0 + r) * a.num_q_heads + my.h) * kD;
+            if (32 * q + 32 <= my.rows) {
+                // All 32 rows of the warp are the sequence's: stage them in this
+                // sub-tile's Q buffer (every MMA reading it has completed) as two
+                // 64-column boxes of 32 swizzled 128-byte rows, and let TMA store
+                // them -- coalesced, and off the warp's instruction stream.
+                uint8_t *stg = smem + kQOff + (2 * qb + k) * kQBytes + q * 8192;
 #pragma unroll
-                for (int i = 0; i < kD; i += 8) {
-                    const uint4 pk = make_uint4(pack_bf16x2(o[i] * inv, o[i + 1] * inv),
-                                                pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
-                                                pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
-                                                pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
-                    *reinterpret_cast<uint4 *>(orow + i) = pk;
+                for (int j = 0; j < kD / 8; ++j) {
+                    const uint4 pk = make_uint4(pack_bf16x2(o[8 * j] * inv, o[8 * j + 1] * inv),
+                                                pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv),
+                                                pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv),
+                                                pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
+                    *reinterpret_cast<uint4 *>(stg + (j >> 3) * 4096 + lane * 128 + (((j & 7) ^ (lane & 7)) << 4)) =
+                        pk;
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int row = u.row0 + my.q0 + 32 * q;
+                    tma_store_3d(&tm_o, stg, 0, my.h, row);
+                    tma_store_3d(&tm_o, stg + 4096, 64, my.h, row);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(&q_free[qb]);
+                }
+            } else {
+                if (r < my.rows) {
+                    __nv_bfloat16 *orow = a.out + ((size_t)(u.row0 + my.q0 + r) * a.num_q_heads + my.h) * kD;
+#pragma unroll
+                    for (int i = 0; i < kD; i += 8) {
+                        const uint4 pk = make_uint4(pack_bf16x2(o[i] * inv, o[i + 1] * inv),
+                                                    pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
+                                                    pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
+                                                    pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
+                        *reinterpret_cast<uint4 *>(orow + i) = pk;
+                    }
+                }
+                if (lane == 0) mbar_arrive(&q_free[qb]);
             }
         }
+        if (lane == 0) bulk_wait_all();  // the output stores are done before the CTA exits
         if (!ok) atomicExch(s_abort, 1);
     }
     tc_fence_before();
@@ -714,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int BS, bool PAGED, int MODE>
 cudaError_t launch_pair_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                          const PrefillArgs &a, cudaStream_t stream) {
+                          const CUtensorMap &tm_o, const PrefillArgs &a, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<BS, PAGED, MODE>,
@@ -726,25 +762,26 @@ cudaError_t launch_pair_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, cons
                             (a.num_q_heads / heads_per_pair(MODE)) * a.num_seqs;
     if (units == 0) return cudaSuccess;
     const int pairs = (int)std::min<long long>(units, std::max(1, a.num_sms / 2));
-    prefill_pair_kernel<BS, PAGED, MODE><<<dim3(2 * pairs), kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a);
+    prefill_pair_kernel<BS, PAGED, MODE><<<dim3(2 * pairs), kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_o,
+                                                                                        a);
     return cudaGetLastError();
 }
 
 template <int BS, bool PAGED>
 cudaError_t launch_pair_m(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                          const PrefillArgs &a, cudaStream_t stream) {
-    if (a.group % 4 == 0) return launch_pair_t<BS, PAGED, 0>(tm_q, tm_k, tm_v, a, stream);
-    if (a.group % 2 == 0) return launch_pair_t<BS, PAGED, 1>(tm_q, tm_k, tm_v, a, stream);
-    return launch_pair_t<BS, PAGED, 2>(tm_q, tm_k, tm_v, a, stream);
+                          const CUtensorMap &tm_o, const PrefillArgs &a, cudaStream_t stream) {
+    if (a.group % 4 == 0) return launch_pair_t<BS, PAGED, 0>(tm_q, tm_k, tm_v, tm_o, a, stream);
+    if (a.group % 2 == 0) return launch_pair_t<BS, PAGED, 1>(tm_q, tm_k, tm_v, tm_o, a, stream);
+    return launch_pair_t<BS, PAGED, 2>(tm_q, tm_k, tm_v, tm_o, a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_pair(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                const PrefillArgs &a, int block_size, cudaStream_t stream) {
-    if (a.block_table == nullptr) return launch_pair_m<16, false>(tm_q, tm_k, tm_v, a, stream);
-    if (block_size == 16) return launch_pair_m<16, true>(tm_q, tm_k, tm_v, a, stream);
-    if (block_size == 32) return launch_pair_m<32, true>(tm_q, tm_k, tm_v, a, stream);
+                                const CUtensorMap &tm_o, const PrefillArgs &a, int block_size, cudaStream_t stream) {
+    if (a.block_table == nullptr) return launch_pair_m<16, false>(tm_q, tm_k, tm_v, tm_o, a, stream);
+    if (block_size == 16) return launch_pair_m<16, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
+    if (block_size == 32) return launch_pair_m<32, true>(tm_q, tm_k, tm_v, tm_o, a, stream);
     return cudaErrorInvalidValue;
 }
 
