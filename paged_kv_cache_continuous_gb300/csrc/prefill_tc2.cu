@@ -593,23 +593,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 else mbar_arrive_cluster(remote);
             }
         };
-        auto row_max = [&](const float *x) {
+        // A row's scores are handled in two halves of 64 keys (64 registers
+        // live instead of 128, which leaves the compiler room to overlap the
+        // exponentials of many columns).
+        auto row_max64 = [&](const float *x) {
             float m4[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) m4[i] = fmax3(x[i], x[i + 4], x[i + 8]);
 #pragma unroll
-            for (int j = 12; j < kBN; j += 8)
+            for (int j = 12; j < 64; j += 8)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[j + i], j + 4 + i < kBN ? x[j + 4 + i] : -INFINITY);
+                for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[j + i], j + 4 + i < 64 ? x[j + 4 + i] : -INFINITY);
             return fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
         };
-        // P_k(t) = exp2(scale * S - mu) as bf16 pairs over the first 64 columns
-        // of S_k (column j: keys 2j, 2j+1); returns the row sum of the same
-        // rounded weights.  The TMEM stores are left in flight.
-        auto exps_to_tmem = [&](const float *x, float mu) {
+        auto mask64 = [&](float *x, int lim) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) x[j] = j < lim ? x[j] : -INFINITY;
+        };
+        // P = exp2(scale * S - mu) for 64 keys as 32 bf16 pairs at TMEM column
+        // `pcol` of S_k (column j: keys 2j, 2j+1 of the half); returns the row
+        // sum of the same rounded weights.  The TMEM stores are left in flight.
+        auto exps64_to_tmem = [&](const float *x, float mu, uint32_t pcol) {
             float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int cq = 0; cq < kBN / 32; ++cq) {
+            for (int cq = 0; cq < 2; ++cq) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -617,9 +624,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                         fast_exp2(fmaf(x[32 * cq + 2 * j + 1], sl, -mu)));
                     ls2[j & 1] = add_f32x2(ls2[j & 1], bf16x2_unpack(pk[j]));
                 }
-                tmem_st16_async(tS + 16 * cq, pk);
+                tmem_st16_async(pcol + 16 * cq, pk);
             }
             return (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
+        };
+        auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+            for (int cc = 0; cc < kD / 32; ++cc) {
+                float o[32];
+                tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                tmem_st32(tO + cc * 32, o);
+            }
         };
         for (int rnd = 0; rnd * pairs < num_units && ok; ++rnd) {
             const int v = unit_of(rnd);
@@ -645,39 +662,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 ++sc;
                 tc_fence_after();
-                float v[kBN];
-                tmem_ld128(tS, v);
                 const int lim = lim_abs - t * kBN;  // visible columns of this row
                 // Warp-uniform branch: only tiles crossing some row's last key pay
                 // for the mask.
-                if (__any_sync(0xffffffffu, lim < kBN)) {
-#pragma unroll
-                    for (int j = 0; j < kBN; ++j) v[j] = j < lim ? v[j] : -INFINITY;
+                const bool masked = __any_sync(0xffffffffu, lim < kBN);
+                if (t == 0) {
+                    // key 0 is visible to every row, so the first tile's maximum is finite
+                    float v[64];
+                    tmem_ld64(tS, v);
+                    if (masked) mask64(v, lim);
+                    float mx = row_max64(v);
+                    tmem_ld64(tS + 64, v);
+                    if (masked) mask64(v, lim - 64);
+                    m_run = fmaxf(mx, row_max64(v)) * sl;
                 }
-                // key 0 is visible to every row, so the first tile's maximum is finite
-                if (t == 0) m_run = row_max(v) * sl;
-                // Exponentials against the running maximum (one copy of the code
-                // for every tile, which keeps it in the instruction cache); the row
-                // sum shows when the maximum has grown too far (weights above 2^64
-                // or not finite): then move it, rescale O_k (stable: PV_k(t-1) has
-                // completed) and redo the tile, once.  Never taken for t == 0.
-                float l_tile;
+                // Exponentials against the running maximum, half by half (P of
+                // keys 0-63 over S columns 0-31, whose scores are read; keys 64-127
+                // over columns 32-63, read with the first half).  A half's row sum
+                // shows when the maximum has grown too far (weights above 2^63 or
+                // not finite; never for t == 0): then move the maximum, rescale O_k
+                // (stable: PV_k(t-1) has completed) and an already written first
+                // half, and redo the half.
+                float l_tile = 0.f;
 #pragma unroll 1
-                for (int pass = 0;; ++pass) {
-                    l_tile = exps_to_tmem(v, m_run);
-                    if (pass > 0 || t == 0 || !__any_sync(0xffffffffu, !(l_tile <= 0x1p64f))) break;
-                    const float m_new = fmaxf(m_run, row_max(v) * sl);
-                    const float alpha = fast_exp2(m_run - m_new);
-                    m_run = m_new;
+                for (int h = 0; h < 2; ++h) {
+                    float v[64];
+                    tmem_ld64(tS + 64 * h, v);
+                    if (masked) mask64(v, lim - 64 * h);
+                    float lh = exps64_to_tmem(v, m_run, tS + 32 * h);
+                    if (t > 0 && __any_sync(0xffffffffu, !(lh <= 0x1p63f))) {
+                        float mx = row_max64(v);
+                        if (h == 0) {  // the second half's scores are still in S columns 64-127
+                            float w[64];
+                            tmem_ld64(tS + 64, w);
+                            if (masked) mask64(w, lim - 64);
+                            mx = fmaxf(mx, row_max64(w));
+                        }
+                        const float m_new = fmaxf(m_run, mx * sl);
+                        const float alpha = fast_exp2(m_run - m_new);
+                        m_run = m_new;
+                        rescale_o(alpha);
+                        l_run *= alpha;
+                        tmem_wait_st();
+                        if (h == 1) {  // the first half's weights, already in TMEM: scale and re-round
+                            uint32_t pk[32];
+                            tmem_ld32(tS, reinterpret_cast<float *>(pk));
+                            float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int cc = 0; cc < kD / 32; ++cc) {
-                        float o[32];
-                        tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tO + cc * 32, o);
+                            for (int j = 0; j < 32; ++j) {
+                                const float2 w2 = bf16x2_unpack(pk[j]);
+                                pk[j] = pack_bf16x2(w2.x * alpha, w2.y * alpha);
+                                ls2 = add_f32x2(ls2, bf16x2_unpack(pk[j]));
+                            }
+                            tmem_st16_async(tS, pk);
+                            tmem_st16_async(tS + 16, pk + 16);
+                            l_tile = ls2.x + ls2.y;
+                        }
+                        lh = exps64_to_tmem(v, m_run, tS + 32 * h);
                     }
-                    l_run *= alpha;
+                    l_tile += lh;
                 }
                 l_run = (t == 0) ? l_tile : l_run + l_tile;
                 tmem_wait_st();
