@@ -448,7 +448,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) atomicExch(s_abort, 1);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // --------------------------------------------------------- MMA issue --
-        if (c == 0 && lane == 0) {
+        // Each issuing warp runs its loop warp-uniformly (descriptors in uniform
+        // registers); one elected lane issues every MMA and commit.
+        if (c == 0) {
             const int k = warp - kMmaWarp;
             constexpr uint32_t kIdescS = umma_idesc_bf16(2 * kBM, kBN, false, false);
             constexpr uint32_t kIdescO = umma_idesc_bf16(2 * kBM, kD, false, true);
@@ -463,21 +465,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // Wait until the other thread has queued `target` groups (a
             // monotone count in shared memory).
             auto wait_count = [&](int target) {
-                if (!ok || turn_cnt[1 - k] >= target) return;
+                if (!ok) return;
                 const long long t0 = clock64();
+                bool good = true;  // every lane spins until it sees the count (monotone)
                 for (uint32_t it = 1;; ++it) {
-                    if (turn_cnt[1 - k] >= target) return;
-                    if ((it & 1023u) == 0) {
-                        if (clock64() - t0 > kWaitLimitCycles) {
-                            set_error(a.err, PA_ERR_TIMEOUT);
-                            ok = false;
-                            return;
-                        }
-                        if (*(volatile int *)a.err == PA_ERR_TIMEOUT) {
-                            ok = false;
-                            return;
-                        }
+                    if (turn_cnt[1 - k] >= target) break;
+                    if ((it & 1023u) == 0 && (clock64() - t0 > kWaitLimitCycles ||
+                                              *(volatile int *)a.err == PA_ERR_TIMEOUT)) {
+                        good = false;
+                        break;
                     }
+                }
+                good = __all_sync(0xffffffffu, good);
+                if (!good) {
+                    if (lane == 0) set_error(a.err, PA_ERR_TIMEOUT);
+                    ok = false;
                 }
             };
             for (int rnd = 0; rnd * pairs < num_units && ok; ++rnd) {
@@ -504,56 +506,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint64_t dq = umma_desc_sw128(smem_u32(smem + kQOff + (2 * qb + k) * kQBytes), 16, 1024);
                 auto wait_tile = [&](int t) {
                     const int gt = gb + t;
-                    if (ok) ok = mbar_wait_spin(&tile_full[gt % kStages], (gt / kStages) & 1, a.err);
+                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_spin(&tile_full[gt % kStages], (gt / kStages) & 1, a.err));
                 };
                 auto issue_s = [&](int t) {  // S_k(t) = Q_k K(t)^T; the caller waited for tile t
                     const uint64_t bk = dk0 + (uint64_t)((((gb + t) % kStages) * kStageBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
-                        umma_bf16_pair(tS, dq + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
+                        umma_bf16_pair_w(tS, dq + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
                                        bk + (uint64_t)(((kk >> 2) * kKHalf + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
                         if (kk == 3) pass_turn();
                     }
                 };
                 if (nk > 0) {
-                    if (ok) ok = mbar_wait_spin(&q_full[qb], (ord >> 1) & 1, a.err);
+                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_spin(&q_full[qb], (ord >> 1) & 1, a.err));
                     wait_tile(0);
                     take_turn(0);
                     if (ok) {
                         issue_s(0);
-                        umma_commit_pair(&s_full[k]);
+                        umma_commit_pair_w(&s_full[k]);
                     }
                 }
                 for (int t = 0; t < nk && ok; ++t) {
                     const bool more = t + 1 < nk;
                     if (more) wait_tile(t + 1);
                     take_turn(t + 1);  // usually passed before P_k(t) is ready
-                    if (!ok || !(ok = mbar_wait_spin(&p_full[k], pc & 1, a.err))) break;
+                    if (!ok || !(ok = __all_sync(0xffffffffu, mbar_wait_spin(&p_full[k], pc & 1, a.err)))) break;
                     ++pc;
-                    if (t == u.T - 1 && !(ok = mbar_wait_spin(&v_tail[ord & 1], (ord >> 1) & 1, a.err))) break;
+                    if (t == u.T - 1 && !(ok = __all_sync(0xffffffffu, mbar_wait_spin(&v_tail[ord & 1], (ord >> 1) & 1, a.err)))) break;
                     // O_k is released by the softmax warps before this unit's first PV_k overwrites it.
-                    if (t == 0 && uo > 0 && !(ok = mbar_wait_spin(&o_free[k], (uo - 1) & 1, a.err))) break;
+                    if (t == 0 && uo > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait_spin(&o_free[k], (uo - 1) & 1, a.err)))) break;
                     tc_fence_after();
                     // O_k += P_k(t) V(t), P_k from TMEM (written by the softmax warps)
                     const uint64_t bv = dv0 + (uint64_t)((((gb + t) % kStages) * kStageBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
-                        umma_bf16_pair_tmem_a(tO, tS + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
+                        umma_bf16_pair_tmem_a_w(tO, tS + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
                                               (t > 0 || kk > 0) ? 1u : 0u);
                         if (kk == 3 && !more) pass_turn();
                     }
                     if (more) issue_s(t + 1);  // overwrites P_k(t): after PV_k(t) in the tensor pipe
                     if (more) {
-                        umma_commit_pair(&s_full[k]);
+                        umma_commit_pair_w(&s_full[k]);
                     } else {
-                        umma_commit_pair(&o_done[k]);
-                        umma_commit_pair(&q_free[qb]);  // this thread's last S of the unit is done
+                        umma_commit_pair_w(&o_done[k]);
+                        umma_commit_pair_w(&q_free[qb]);  // this thread's last S of the unit is done
                     }
-                    umma_commit_pair(&tile_free[(gb + t) % kStages]);
-                    if (t >= nk_other) umma_commit_pair(&tile_free[(gb + t) % kStages]);  // the only reader
+                    umma_commit_pair_w(&tile_free[(gb + t) % kStages]);
+                    if (t >= nk_other) umma_commit_pair_w(&tile_free[(gb + t) % kStages]);  // the only reader
                 }
                 if (!ok) break;
-                if (nk == 0) umma_commit_pair(&q_free[qb]);  // nothing of this thread reads Q buffer qb
+                if (nk == 0) umma_commit_pair_w(&q_free[qb]);  // nothing of this thread reads Q buffer qb
                 else ++uo;
                 gbase[0] += groups[0];
                 gbase[1] += groups[1];
@@ -561,9 +563,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ++ord;
             }
             // Do not let the pair tear down TMEM under MMAs still in flight.
-            umma_commit_pair(&mma_fin[k], 1);
+            umma_commit_pair_w(&mma_fin[k], 1);
             mbar_wait(&mma_fin[k], 0, a.err);
-            if (!ok) atomicExch(s_abort, 1);
+            if (!ok && lane == 0) atomicExch(s_abort, 1);
         }
         __syncwarp();
     } else {
