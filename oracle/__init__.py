@@ -16,6 +16,10 @@ the passage it follows, is written beside the C function it wraps:
   optional cached prefix read through the block table.
 * ``mixed_step``     -- append, then decode for the first ``num_decode``
   sequences and prefill for the rest.
+* ``rope``           -- rotary position embedding of head vectors.
+* ``rope_append``    -- rotate the new tokens' queries and keys, then append
+  the rotated keys (rounded to bf16) and the values to the pool.
+* ``to_bf16``        -- round doubles to bf16 bit patterns.
 
 Parity pins: tests/test_oracle_pins.py checks these functions against a
 library routine (torch's scaled-dot-product attention in float64 on dense
@@ -75,8 +79,10 @@ def _load():
         lib.oracle_expected_slots.argtypes = [I, P, P, P, I, I, P]
         lib.oracle_decode.argtypes = [I, I, I, I, I, I, D, P, P, P, P, I, P, P, I, P, I]
         lib.oracle_prefill.argtypes = [I, I, I, I, I, I, D, P, P, P, P, P, P, I, P, I, P, I]
+        lib.oracle_rope.argtypes = [I, I, I, P, P, D, P]
+        lib.oracle_to_bf16.argtypes = [ctypes.c_longlong, P, P]
         for f in (lib.oracle_kv_append, lib.oracle_expected_slots,
-                  lib.oracle_decode, lib.oracle_prefill):
+                  lib.oracle_decode, lib.oracle_prefill, lib.oracle_rope, lib.oracle_to_bf16):
             f.restype = I
         _lib = lib
     return _lib
@@ -256,3 +262,37 @@ def mixed_step(q, k_new, v_new, q_start_loc, seq_lens, slot_mapping, block_table
         out[r0:r1] = prefill(q[r0:r1], kp, vp, cu, prefix_lens=pre, block_table=bt[nd:],
                              scale=scale, threads=threads)
     return out, kp, vp
+
+
+def rope(x, positions, theta: float = 10000.0) -> np.ndarray:
+    """fp64 rotary embedding (oracle.c: ``oracle_rope``).  x: uint16 bits
+    [T, H, d]; positions: int32 [T].  Returns float64 [T, H, d]."""
+    xb = _u16(x)
+    if xb.ndim != 3:
+        raise ValueError("x must be [T, H, d]")
+    T, H, d = xb.shape
+    pos = _i32(positions)
+    if pos.shape != (T,):
+        raise ValueError("positions must be [T]")
+    out = np.zeros((T, H, d), dtype=np.float64)
+    _check(_load().oracle_rope(T, H, d, _ptr(xb), _ptr(pos), ctypes.c_double(float(theta)), _ptr(out)), "rope")
+    return out
+
+
+def to_bf16(x) -> np.ndarray:
+    """Round float64 values to bf16 bit patterns (ties to even)."""
+    xa = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.zeros(xa.shape, dtype=np.uint16)
+    _check(_load().oracle_to_bf16(ctypes.c_longlong(xa.size), _ptr(xa), _ptr(out)), "to_bf16")
+    return out
+
+
+def rope_append(q, k_new, v_new, positions, slot_mapping, k_pool, v_pool, theta: float = 10000.0):
+    """The new tokens' queries and keys rotated (``rope``), the rotated keys
+    rounded to bf16 and appended with the values (``kv_append``).  Returns
+    (q_rot float64, k_rot float64, k_pool, v_pool)."""
+    q_rot = rope(q, positions, theta)
+    k_rot = rope(k_new, positions, theta)
+    k_pool2, v_pool2 = kv_append(to_bf16(k_rot), v_new, slot_mapping, k_pool, v_pool)
+    return q_rot, k_rot, k_pool2, v_pool2
+

@@ -398,3 +398,71 @@ int oracle_prefill(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
     long long n = pairs ? num_pairs : (long long)cu_seqlens_q[num_seqs] * num_q_heads;
     return run_items(prefill_item, &pc, n, nthreads, (size_t)max_len + 1, head_dim);
 }
+
+/*
+ * Rotary position embedding of the new tokens' queries and keys.  The pages
+ * only name the flashinfer build option that compiles its position-encoding
+ * modes in; the plainest reading of "the" rotary embedding there is the one
+ * of Su et al. (RoFormer, 2021) with the pairing of its Llama / GPT-NeoX
+ * implementations: for a head vector x of even length d at position p, and
+ * i < d/2, with f_i = theta^(-2i/d),
+ *     y[i]       = x[i] cos(p f_i) - x[i + d/2] sin(p f_i)
+ *     y[i + d/2] = x[i + d/2] cos(p f_i) + x[i] sin(p f_i).
+ * x: bf16 bits [T][H][d]; pos: [T]; out: double [T][H][d].
+ */
+int oracle_rope(int num_tokens, int num_heads, int head_dim, const uint16_t *x, const int32_t *pos,
+                double theta, double *out) {
+    if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0 || (head_dim & 1) || !(theta > 0.0)) return OR_ERR_ARG;
+    const int half = head_dim / 2;
+    for (int t = 0; t < num_tokens; ++t) {
+        if (pos[t] < 0) return OR_ERR_ARG;
+        for (int i = 0; i < half; ++i) {
+            const double f = pow(theta, -2.0 * (double)i / (double)head_dim);
+            const double a = (double)pos[t] * f;
+            const double c = cos(a), s = sin(a);
+            for (int h = 0; h < num_heads; ++h) {
+                const size_t base = ((size_t)t * num_heads + h) * head_dim;
+                const double x0 = bf16_to_double(x[base + i]), x1 = bf16_to_double(x[base + i + half]);
+                out[base + i] = x0 * c - x1 * s;
+                out[base + i + half] = x1 * c + x0 * s;
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * Round doubles to bf16 (8 significant bits, round to nearest, ties to even),
+ * directly from double (no intermediate float rounding).  Values past the
+ * bf16 range become infinities; NaN stays NaN.
+ */
+int oracle_to_bf16(long long n, const double *x, uint16_t *out) {
+    for (long long j = 0; j < n; ++j) {
+        const double v = x[j];
+        uint16_t sign = signbit(v) ? 0x8000u : 0u;
+        if (isnan(v)) {
+            out[j] = 0x7fc0u;
+            continue;
+        }
+        double a = fabs(v);
+        if (a == 0.0) {
+            out[j] = sign;
+            continue;
+        }
+        int e;
+        (void)frexp(a, &e);  /* a = m 2^e, m in [0.5, 1) */
+        /* quantum: 2^(e - 8) for normals; bf16's smallest step is 2^-133 */
+        int qexp = e - 8;
+        if (qexp < -133) qexp = -133;
+        double r = ldexp(nearbyint(ldexp(a, -qexp)), qexp);
+        if (r >= 0x1p128) {
+            out[j] = (uint16_t)(sign | 0x7f80u);
+            continue;
+        }
+        float f = (float)r;  /* exact: r has at most 8 significant bits */
+        uint32_t bits;
+        memcpy(&bits, &f, 4);
+        out[j] = (uint16_t)(sign | ((bits >> 16) & 0x7fffu));
+    }
+    return OR_OK;
+}

@@ -388,6 +388,94 @@ def pin_copy_blocks_errors():
     raise AssertionError("overlapping source and destination accepted")
 
 
+# ---------------------------------------------------------------------------
+# Rotary position embedding (RoFormer; Llama / GPT-NeoX pairing) and bf16 rounding
+# ---------------------------------------------------------------------------
+
+def _rope_case(seed, T=5, H=3, d=16):
+    g = torch.Generator().manual_seed(seed)
+    x = wl.bf16_randn((T, H, d), g)
+    pos = np.array([0, 1, 7, 1000, 32767][:T], dtype=np.int32)
+    return bits(x), pos
+
+
+def _f64(b):
+    """bf16 bit patterns -> float64 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_rope_identity_at_position_zero():
+    """Position 0 rotates by nothing: the result is the input, exactly."""
+    xb, _ = _rope_case(1)
+    out = oracle.rope(xb, np.zeros(xb.shape[0], dtype=np.int32))
+    assert np.array_equal(out, _f64(xb))
+
+
+def pin_rope_is_complex_rotation():
+    """Pair (i, i + d/2) as the complex number x_i + j x_{i+d/2}: the embedding
+    multiplies it by exp(j p theta^(-2i/d)) (numpy complex arithmetic)."""
+    xb, pos = _rope_case(2)
+    T, H, d = xb.shape
+    x = _f64(xb)
+    half = d // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    ang = pos[:, None].astype(np.float64) * np.power(10000.0, -np.arange(half) * 2.0 / d)[None, :]
+    w = z * np.exp(1j * ang)[:, None, :]
+    ref = np.concatenate([w.real, w.imag], axis=-1)
+    np.testing.assert_allclose(oracle.rope(xb, pos), ref, rtol=0, atol=1e-12)
+
+
+def pin_rope_relative_position():
+    """The defining property: <R(m) q, R(n) k> depends on m - n only."""
+    g = torch.Generator().manual_seed(3)
+    q, k = bits(wl.bf16_randn((1, 1, 64), g)), bits(wl.bf16_randn((1, 1, 64), g))
+    dots = []
+    for shift in (0, 5, 1234):
+        qr = oracle.rope(q, np.array([17 + shift], np.int32))
+        kr = oracle.rope(k, np.array([9 + shift], np.int32))
+        dots.append(float((qr * kr).sum()))
+    assert max(dots) - min(dots) < 1e-9, dots
+
+
+def pin_to_bf16_rounding():
+    """Round to nearest, ties to the even significand: every value is checked
+    against the nearest of all bf16 numbers near it, in exact rational
+    arithmetic (brute force)."""
+    from fractions import Fraction
+    vals = [1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8 + 2.0 ** -20), 3.14159, 1e-30,
+            -7.5e5, 2.0 ** -126 * 1.5, 0.0, 255.5, 256.5]
+    got = oracle.to_bf16(np.array(vals))
+    for v, b in zip(vals, got):
+        if v == 0.0:
+            assert b == 0
+            continue
+        fv = abs(Fraction(v))
+        e = fv.numerator.bit_length() - fv.denominator.bit_length()
+        # candidates m * 2^(ee - 7), significand m in [128, 256)
+        cands = [(Fraction(m) * Fraction(2) ** (ee - 7), m) for ee in range(e - 2, e + 3) for m in range(128, 256)]
+        dist = min(abs(c - fv) for c, _ in cands)
+        near = [(c, m) for c, m in cands if abs(c - fv) == dist]
+        best = near[0][0] if len(near) == 1 else [c for c, m in near if m % 2 == 0][0]
+        want = int(np.float32(float(best)).view(np.uint32)) >> 16 | (0x8000 if v < 0 else 0)
+        assert int(b) == want, (v, hex(int(b)), hex(want))
+
+
+def pin_rope_append_pool():
+    """The pool receives the rotated keys rounded to bf16 and the values bit
+    for bit; the rotated queries are returned unrounded."""
+    shape = wl.Shape(num_q_heads=4, num_kv_heads=2, head_dim=16, block_size=4, num_blocks=8)
+    g = torch.Generator().manual_seed(4)
+    q, k, v = (bits(wl.bf16_randn((3, h, 16), g)) for h in (4, 2, 2))
+    kp, vp = wl.new_pool(shape, 5)
+    slots = np.array([5, 0, 13], np.int32)
+    pos = np.array([2, 3, 40], np.int32)
+    q_rot, k_rot, kp2, vp2 = oracle.rope_append(q, k, v, pos, slots, bits(kp), bits(vp))
+    np.testing.assert_allclose(q_rot, oracle.rope(q, pos), rtol=0, atol=0)
+    for i, sl in enumerate(slots):
+        assert np.array_equal(kp2[sl // 4, :, sl % 4], oracle.to_bf16(k_rot[i]))
+        assert np.array_equal(vp2[sl // 4, :, sl % 4], v[i])
+
+
 ALL_PINS = [
     pin_decode_vs_sdpa, pin_prefill_dense_vs_sdpa, pin_prefill_paged_vs_sdpa,
     pin_chunked_prefill_vs_sdpa, pin_append_layout, pin_append_errors,
@@ -395,5 +483,6 @@ ALL_PINS = [
     pin_zero_query_is_mean, pin_dominant_key, pin_two_key_golden,
     pin_block_permutation_invariance, pin_decode_equals_prefill_row,
     pin_mixed_step_composition, pin_copy_blocks_fork_vs_sdpa, pin_copy_blocks_swap_round_trip,
-    pin_copy_blocks_errors,
+    pin_copy_blocks_errors, pin_rope_identity_at_position_zero, pin_rope_is_complex_rotation,
+    pin_rope_relative_position, pin_to_bf16_rounding, pin_rope_append_pool,
 ]

@@ -31,6 +31,10 @@ MUTATIONS = [
     ("slot_formula_wrong", "slots_out[q_start[s] + i] = blk * block_size + p % block_size;",
      "slots_out[q_start[s] + i] = blk * block_size + p / block_size;", 1),
     ("dup_check_dropped", "if (seen[slot]) { free(seen); return OR_ERR_SLOT_DUP; }", "", 1),
+    ("rope_sign", "out[base + i] = x0 * c - x1 * s;", "out[base + i] = x0 * c + x1 * s;", 1),
+    ("rope_interleaved_pairs", "x1 = bf16_to_double(x[base + i + half]);", "x1 = bf16_to_double(x[base + (i ^ 1)]);", 1),
+    ("rope_frequency", "pow(theta, -2.0 * (double)i / (double)head_dim)", "pow(theta, -1.0 * (double)i / (double)head_dim)", 1),
+    ("bf16_truncates", "nearbyint(ldexp(a, -qexp))", "floor(ldexp(a, -qexp))", 1),
 ]
 
 
