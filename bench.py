@@ -245,6 +245,7 @@ def run_ours(args, world, rank, local):
     # ---- prefill half of the metric (tensor cores), timed alone with L2 flushed
     prefill = measure_prefill(pa, wl, dev, bf16_peak, peak_src, args.prefill_iters) if rank == 0 else None
     copy = measure_copy(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
+    rope = measure_rope(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
 
     clocks = clk.summary()
     traffic = load_traffic("decode_splitk", nbytes, st.num_seqs)
@@ -272,6 +273,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "prefill": prefill,
         "block_copy": copy,
+        "rope_append": rope,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kp, vp, st, split, args.cpu_seconds)
@@ -460,6 +462,43 @@ def measure_copy(pa, wl, dev, hbm_peak, iters):
                                      "bytes": "K+V moved to pinned host"},
             "swap_in_1024_blocks": {"ms": round(t_in * 1e3, 4), "GBps": round(swap_b / t_in / 1e9, 1),
                                     "bytes": "K+V moved from pinned host"}}
+
+
+def measure_rope(pa, wl, dev, hbm_peak, iters):
+    """Rotary embedding fused with the append (pa_rope_append), L2 flushed
+    before each launch: a 4096-token prompt step (Hq 32, Hkv 8, d 128) and the
+    decode step's 128 tokens (Hq = Hkv = 32).  Bytes: q read and written, k and
+    v read and written to the pool, positions and slots read."""
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    res = {}
+    for name, T, Hq, Hkv in (("prompt_4096", 4096, 32, 8), ("decode_step_128", 128, 32, 32)):
+        g = torch.Generator().manual_seed(23)
+        nb = T // 16 + 16
+        shape = wl.Shape(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, block_size=16, num_blocks=nb)
+        q = wl.bf16_randn((T, Hq, 128), g).to(dev)
+        k, v = wl.bf16_randn((T, Hkv, 128), g).to(dev), wl.bf16_randn((T, Hkv, 128), g).to(dev)
+        kp = torch.zeros((nb, Hkv, 16, 128), dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros_like(kp)
+        pos = torch.arange(T, dtype=torch.int32, device=dev)
+        slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int32).to(dev)
+        q_out = torch.empty_like(q)
+        for _ in range(3):
+            pa.rope_append(shape, q, k, v, pos, slots, kp, vp, q_out=q_out)
+        pa.check_device_error()
+        ts = []
+        for _ in range(iters):
+            flush.add_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            pa.rope_append(shape, q, k, v, pos, slots, kp, vp, q_out=q_out)
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        t = float(np.median([x.elapsed_time(y) for x, y in ts])) / 1e3
+        nbytes = T * (Hq + 2 * Hkv) * 128 * 2 * 2 + 8 * T
+        res[name] = {"tokens": T, "ms": round(t * 1e3, 4), "GBps": round(nbytes / t / 1e9, 1),
+                     "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 4)}
+    return {"kernel": "rope_append_kernel", "l2": "flushed (256 MB write) before each launch", **res}
 
 
 # ------------------------------------------------------------ CPU oracle --

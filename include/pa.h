@@ -202,6 +202,29 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
                       int num_seqs, int max_seq_len, void *out, void *stream);
 
 /*
+ * Rotary position embedding of a step's new tokens, fused with their KV
+ * append (the position-encoding mode the pages' flashinfer build compiles in,
+ * Blitzscale docs, section "Build"; the rotation of RoFormer with the Llama /
+ * GPT-NeoX pairing): for token t at position p = positions[t], every query
+ * head row and key head row x (length d) becomes, for i < d/2 and
+ * f_i = theta^(-2i/d),
+ *     y[i] = x[i] cos(p f_i) - x[i+d/2] sin(p f_i),
+ *     y[i+d/2] = x[i+d/2] cos(p f_i) + x[i] sin(p f_i)   (rounded to bf16).
+ * q [T][Hq][d] -> q_out [T][Hq][d] (q_out == q rotates in place); the rotated
+ * k [T][Hkv][d] and v (unchanged) go to slot_mapping[t] of the pools exactly
+ * as pa_kv_append writes them (slot < 0: no append for that token; its query
+ * is still rotated).  Decode and prefill then take q_out and the pools as
+ * usual.  rope_theta: 0 means 10000.  A negative position or a slot past the
+ * pool sets the error word and that token (resp. its append) is skipped.
+ * Returns PA_ERR_INVALID_ARG for NULL / misaligned pointers, num_tokens < 0
+ * or a negative or infinite rope_theta; asynchronous on `stream`; the caller owns every
+ * buffer.
+ */
+int pa_rope_append(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                   const int32_t *positions, const int32_t *slot_mapping, int num_tokens,
+                   float rope_theta, void *q_out, void *k_pool, void *v_pool, void *stream);
+
+/*
  * Copy whole KV blocks between two pools of the same shape (num_kv_heads,
  * block_size, head_dim; shape->num_blocks is not used here):
  *     dst_k[dst_ids[i]] = src_k[src_ids[i]],  dst_v alike,  0 <= i < num_pairs

@@ -29,7 +29,7 @@ ERR_TIMEOUT = 7
 EXPORTS = [
     "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode",
     "pa_decode_noalloc", "pa_prefill",
-    "pa_mixed_step", "pa_copy_blocks", "pa_set_validation", "pa_check_device_error", "pa_last_error",
+    "pa_mixed_step", "pa_copy_blocks", "pa_rope_append", "pa_set_validation", "pa_check_device_error", "pa_last_error",
     "pa_set_decode_split",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
     "pa_alloc_num_free", "pa_alloc_num_blocks_of", "pa_alloc_block_table",
@@ -77,6 +77,7 @@ def load():
         "pa_prefill": ([SP, P, P, P, P, P, P, I, I, I, I, P, P], I),
         "pa_mixed_step": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P], I),
         "pa_copy_blocks": ([SP, P, P, I, P, P, I, P, P, I, P], I),
+        "pa_rope_append": ([SP, P, P, P, P, P, I, ctypes.c_float, P, P, P, P], I),
         "pa_set_validation": ([I], I),
         "pa_check_device_error": ([P], I),
         "pa_last_error": ([], ctypes.c_char_p),
@@ -179,6 +180,21 @@ def copy_blocks(shape, src_k, src_v, dst_k, dst_v, src_ids, dst_ids, stream=None
                                  int(src_k.shape[0]), _bf16(dst_k, "dst_k"), _bf16(dst_v, "dst_v"),
                                  int(dst_k.shape[0]), _i32(src_ids, "src_ids"), _i32(dst_ids, "dst_ids"), n,
                                  _stream(stream)))
+
+
+def rope_append(shape, q, k_new, v_new, positions, slot_mapping, k_pool, v_pool, q_out=None,
+                theta: float = 10000.0, stream=None) -> torch.Tensor:
+    """pa_rope_append: rotate the new tokens' queries (into q_out, a new tensor
+    unless given; pass q to rotate in place) and keys, and append the rotated
+    keys and the values to the pools.  Returns q_out."""
+    T = int(slot_mapping.shape[0])
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    _check(load().pa_rope_append(ctypes.byref(_shape(shape)), _bf16(q, "q"), _bf16(k_new, "k_new"),
+                                 _bf16(v_new, "v_new"), _i32(positions, "positions"),
+                                 _i32(slot_mapping, "slot_mapping"), T, float(theta), _bf16(q_out, "q_out"),
+                                 _bf16(k_pool, "k_pool"), _bf16(v_pool, "v_pool"), _stream(stream)))
+    return q_out
 
 
 def decode(shape, q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, out=None,

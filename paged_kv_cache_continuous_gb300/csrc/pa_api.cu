@@ -372,6 +372,56 @@ int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new, 
     return ok();
 }
 
+int pa_rope_append(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                   const int32_t *positions, const int32_t *slot_mapping, int num_tokens, float rope_theta,
+                   void *q_out, void *k_pool, void *v_pool, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (!(rope_theta >= 0.f) || std::isinf(rope_theta)) return fail(PA_ERR_INVALID_ARG, "rope_theta must be finite, >= 0");
+    if (num_tokens == 0) return ok();
+    if (!q || !k_new || !v_new || !positions || !slot_mapping || !q_out || !k_pool || !v_pool)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out) || !aligned16(k_pool) ||
+        !aligned16(v_pool))
+        return fail(PA_ERR_INVALID_ARG, "q, k/v, q_out and pools must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.slot_mapping = slot_mapping;
+        ca.num_tokens = num_tokens;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    RopeArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.positions = positions;
+    a.slot_mapping = slot_mapping;
+    a.q_out = static_cast<__nv_bfloat16 *>(q_out);
+    a.k_pool = static_cast<__nv_bfloat16 *>(k_pool);
+    a.v_pool = static_cast<__nv_bfloat16 *>(v_pool);
+    a.err = d->err;
+    a.num_tokens = num_tokens;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.head_dim = shape->head_dim;
+    a.block_size = shape->block_size;
+    a.num_blocks = shape->num_blocks;
+    a.check_err_first = val;
+    const double theta = rope_theta == 0.f ? 10000.0 : (double)rope_theta;
+    for (int i = 0; i < shape->head_dim / 2; ++i) a.inv_freq[i] = pow(theta, -2.0 * i / shape->head_dim);
+    cudaError_t e = launch_rope_append(a, d->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rope_append launch");
+    return ok();
+}
+
 int pa_copy_blocks(const pa_shape_t *shape, const void *src_k, const void *src_v, int src_num_blocks,
                    void *dst_k, void *dst_v, int dst_num_blocks, const int32_t *src_ids,
                    const int32_t *dst_ids, int num_pairs, void *stream) {

@@ -40,6 +40,18 @@ cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_
                              cudaStream_t stream);
 
 // Whole-block copies between pools (device or pinned host memory).
+// Rotary embedding of a step's new tokens fused with their KV append.
+struct RopeArgs {
+    const __nv_bfloat16 *q, *k_new, *v_new;
+    const int32_t *positions, *slot_mapping;
+    __nv_bfloat16 *q_out, *k_pool, *v_pool;
+    int *err;
+    int num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+    int check_err_first;
+    double inv_freq[64];  // theta^(-2i/d), i < d/2
+};
+cudaError_t launch_rope_append(const RopeArgs &a, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
                                const int32_t *src_ids, const int32_t *dst_ids, int num_pairs,
                                long long block_bytes, int src_blocks, int dst_blocks, int num_sms, int *err,

@@ -1,0 +1,125 @@
+// rope.cu -- rotary position embedding of a step's new tokens, fused with the
+// KV append: one pass over the new tokens rotates their queries (into q_out,
+// which the decode / prefill kernels then read) and their keys (written
+// straight into the pool slot), and copies their values.
+//
+// The pages name only the flashinfer build option that compiles its
+// position-encoding modes in (Blitzscale docs, section "Build"); the rotation
+// is the RoFormer one with the Llama / GPT-NeoX pairing: for a head vector x
+// of length d at position p and i < d/2, with f_i = theta^(-2i/d),
+//     y[i]       = x[i] cos(p f_i) - x[i + d/2] sin(p f_i)
+//     y[i + d/2] = x[i + d/2] cos(p f_i) + x[i] sin(p f_i).
+// The frequencies come from the host in double; p f_i is formed and reduced
+// modulo 2 pi in double, so cos / sin are taken (in float) of an angle in
+// [-pi, pi] whatever the position; the rotation is float, rounded to bf16.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTok = 4;  // tokens per CTA pass: their cos / sin first, then all their rows at once
+
+// Rotate eight pairs (i .. i+7 with i+d/2 .. i+d/2+7) of one head row: lo / hi
+// are 8 bf16 each (16 bytes); cs holds (cos, sin) of the eight pairs.
+__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float2 *cs) {
+    __nv_bfloat162 *l = reinterpret_cast<__nv_bfloat162 *>(&lo);
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&hi);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 a = __bfloat1622float2(l[j]), b = __bfloat1622float2(h[j]);
+        const float2 c0 = cs[2 * j], c1 = cs[2 * j + 1];  // (cos, sin) of pairs 2j, 2j+1
+        const float y0 = fmaf(a.x, c0.x, -b.x * c0.y), y1 = fmaf(a.y, c1.x, -b.y * c1.y);
+        const float z0 = fmaf(b.x, c0.x, a.x * c0.y), z1 = fmaf(b.y, c1.x, a.y * c1.y);
+        l[j] = __floats2bfloat162_rn(y0, y1);
+        h[j] = __floats2bfloat162_rn(z0, z1);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    rope_append_kernel(const RopeArgs a, int tpc) {  // tpc <= kTok tokens per pass
+    __shared__ float2 cs[kTok][64];  // (cos, sin) per token of the pass and pair
+    __shared__ int s_slot[kTok];     // the token's slot, or -1 if it is not appended (or skipped)
+    __shared__ int s_pos_ok[kTok];
+    if (a.check_err_first && *(volatile int *)a.err != 0) return;
+    const int d = a.head_dim, half = d / 2;
+    const int cpr = half / 8;  // 16-byte chunks per half row
+    const long long num_slots = (long long)a.num_blocks * a.block_size;
+    for (int t0 = blockIdx.x * tpc; t0 < a.num_tokens; t0 += gridDim.x * tpc) {
+        const int nt = min(tpc, a.num_tokens - t0);
+        __syncthreads();  // the previous pass's tables are no longer read
+        for (int e = threadIdx.x; e < nt * half; e += kThreads) {
+            const int tt = e / half, i = e % half;
+            const int p = __ldg(a.positions + t0 + tt);
+            double ang = (double)max(p, 0) * a.inv_freq[i];
+            ang -= rint(ang * 0.15915494309189535) * 6.283185307179586;  // into [-pi, pi]
+            float sn, cn;
+            sincosf((float)ang, &sn, &cn);
+            cs[tt][i] = make_float2(cn, sn);
+            if (i == 0) {
+                const int sl = __ldg(a.slot_mapping + t0 + tt);
+                const bool pos_ok = p >= 0, slot_ok = (long long)sl < num_slots;
+                if (!pos_ok || !slot_ok) set_error(a.err, PA_ERR_BAD_INDEX);
+                s_pos_ok[tt] = pos_ok;
+                s_slot[tt] = (pos_ok && slot_ok) ? sl : -1;  // never write outside the pool
+            }
+        }
+        __syncthreads();
+        // queries: nt tokens x Hq rows x cpr chunk pairs
+        const int nq = nt * a.num_q_heads * cpr;
+        for (int e = threadIdx.x; e < nq; e += kThreads) {
+            const int tt = e / (a.num_q_heads * cpr), r = e % (a.num_q_heads * cpr);
+            if (!s_pos_ok[tt]) continue;
+            const int h = r / cpr, i = (r % cpr) * 8;
+            const size_t o = ((size_t)(t0 + tt) * a.num_q_heads + h) * d + i;
+            uint4 lo = *reinterpret_cast<const uint4 *>(a.q + o), hi = *reinterpret_cast<const uint4 *>(a.q + o + half);
+            rotate8(lo, hi, &cs[tt][i]);
+            *reinterpret_cast<uint4 *>(a.q_out + o) = lo;
+            *reinterpret_cast<uint4 *>(a.q_out + o + half) = hi;
+        }
+        // keys, rotated into the slot, and values, copied: nt tokens x Hkv rows
+        const int nk = nt * a.num_kv_heads * cpr;
+        for (int e = threadIdx.x; e < 2 * nk; e += kThreads) {
+            const bool is_v = e >= nk;
+            const int ee = is_v ? e - nk : e;
+            const int tt = ee / (a.num_kv_heads * cpr), r = ee % (a.num_kv_heads * cpr);
+            const int sl = s_slot[tt];
+            if (sl < 0) continue;
+            const int h = r / cpr, i = (r % cpr) * 8;
+            const size_t src = ((size_t)(t0 + tt) * a.num_kv_heads + h) * d + i;
+            const long long blk = sl / a.block_size, off = sl % a.block_size;
+            const size_t dst = ((size_t)(blk * a.num_kv_heads + h) * a.block_size + off) * d + i;
+            if (is_v) {
+                *reinterpret_cast<uint4 *>(a.v_pool + dst) = *reinterpret_cast<const uint4 *>(a.v_new + src);
+                *reinterpret_cast<uint4 *>(a.v_pool + dst + half) =
+                    *reinterpret_cast<const uint4 *>(a.v_new + src + half);
+            } else {
+                uint4 lo = *reinterpret_cast<const uint4 *>(a.k_new + src);
+                uint4 hi = *reinterpret_cast<const uint4 *>(a.k_new + src + half);
+                rotate8(lo, hi, &cs[tt][i]);
+                *reinterpret_cast<uint4 *>(a.k_pool + dst) = lo;
+                *reinterpret_cast<uint4 *>(a.k_pool + dst + half) = hi;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_append(const RopeArgs &a, int num_sms, cudaStream_t stream) {
+    // Small steps (a decode step's few tokens) take one token per pass, so that
+    // they still spread over many SMs; large ones four.
+    const int tpc = a.num_tokens >= num_sms * 8 ? kTok : 1;
+    const int chunks = (a.num_tokens + tpc - 1) / tpc;
+    const int blocks = std::max(1, std::min(chunks, num_sms * 8));
+    rope_append_kernel<<<blocks, kThreads, 0, stream>>>(a, tpc);
+    return cudaGetLastError();
+}
+
+}  // namespace pa
