@@ -20,6 +20,9 @@ the passage it follows, is written beside the C function it wraps:
 * ``rope_append``    -- rotate the new tokens' queries and keys, then append
   the rotated keys (rounded to bf16) and the values to the pool.
 * ``to_bf16``        -- round doubles to bf16 bit patterns.
+* ``e4m3_from_float``, ``e4m3_to_double`` -- fp8 (e4m3) codes.
+* ``kv_append_fp8``  -- append with quantisation to e4m3 (one scale per KV head).
+* ``decode_fp8``     -- decode over e4m3 code pools (value = code * scale).
 
 Parity pins: tests/test_oracle_pins.py checks these functions against a
 library routine (torch's scaled-dot-product attention in float64 on dense
@@ -81,8 +84,14 @@ def _load():
         lib.oracle_prefill.argtypes = [I, I, I, I, I, I, D, P, P, P, P, P, P, I, P, I, P, I]
         lib.oracle_rope.argtypes = [I, I, I, P, P, D, P]
         lib.oracle_to_bf16.argtypes = [ctypes.c_longlong, P, P]
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_longlong, P, P]
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_longlong, P, P]
+        lib.oracle_kv_append_fp8.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P]
+        lib.oracle_decode_fp8.argtypes = [I, I, I, I, I, I, D, P, P, P, P, P, P, I, P, P, I, P, I]
         for f in (lib.oracle_kv_append, lib.oracle_expected_slots,
-                  lib.oracle_decode, lib.oracle_prefill, lib.oracle_rope, lib.oracle_to_bf16):
+                  lib.oracle_decode, lib.oracle_prefill, lib.oracle_rope, lib.oracle_to_bf16,
+                  lib.oracle_e4m3_from_float, lib.oracle_e4m3_to_double, lib.oracle_kv_append_fp8,
+                  lib.oracle_decode_fp8):
             f.restype = I
         _lib = lib
     return _lib
@@ -295,4 +304,59 @@ def rope_append(q, k_new, v_new, positions, slot_mapping, k_pool, v_pool, theta:
     k_rot = rope(k_new, positions, theta)
     k_pool2, v_pool2 = kv_append(to_bf16(k_rot), v_new, slot_mapping, k_pool, v_pool)
     return q_rot, k_rot, k_pool2, v_pool2
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.uint8))
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def e4m3_from_float(x) -> np.ndarray:
+    """float32 values -> e4m3 codes (nearest, ties to even, saturating)."""
+    xa = _f32(x)
+    out = np.zeros(xa.shape, dtype=np.uint8)
+    _check(_load().oracle_e4m3_from_float(ctypes.c_longlong(xa.size), _ptr(xa), _ptr(out)), "e4m3_from_float")
+    return out
+
+
+def e4m3_to_double(codes) -> np.ndarray:
+    c = _u8(codes)
+    out = np.zeros(c.shape, dtype=np.float64)
+    _check(_load().oracle_e4m3_to_double(ctypes.c_longlong(c.size), _ptr(c), _ptr(out)), "e4m3_to_double")
+    return out
+
+
+def kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_pool, v_pool):
+    """Quantising append (oracle.c: ``oracle_kv_append_fp8``).  k_new, v_new:
+    uint16 bf16 bits [T, Hkv, d]; scales float32 [Hkv]; pools uint8 codes
+    [N, Hkv, B, d].  Returns new pools."""
+    kn, vn = _u16(k_new), _u16(v_new)
+    kp, vp = _u8(k_pool).copy(), _u8(v_pool).copy()
+    sl = _i32(slot_mapping)
+    N, H, B, d = kp.shape
+    _check(_load().oracle_kv_append_fp8(sl.shape[0], H, d, B, N, _ptr(kn), _ptr(vn), _ptr(sl),
+                                        _ptr(_f32(k_scale)), _ptr(_f32(v_scale)), _ptr(kp), _ptr(vp)),
+           "kv_append_fp8")
+    return kp, vp
+
+
+def decode_fp8(q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, scale: float = 0.0,
+               pairs=None, threads: int | None = None) -> np.ndarray:
+    """fp64 decode over e4m3 code pools (value = code * scale of the KV
+    head).  q: uint16 [S, Hq, d]; returns float64 [S, Hq, d] or [n, d]."""
+    qb, kp, vp = _u16(q), _u8(k_pool), _u8(v_pool)
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    S, Hq, d = qb.shape
+    N, H, B, _ = kp.shape
+    pr = None if pairs is None else _i32(pairs)
+    n = S * Hq if pr is None else pr.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    _check(_load().oracle_decode_fp8(S, Hq, H, d, B, N, ctypes.c_double(scale), _ptr(qb), _ptr(kp), _ptr(vp),
+                                     _ptr(_f32(k_scale)), _ptr(_f32(v_scale)), _ptr(bt), bt.shape[1], _ptr(sl),
+                                     _ptr(pr), 0 if pr is None else pr.shape[0], _ptr(out),
+                                     threads or default_threads()), "decode_fp8")
+    return out.reshape(S, Hq, d) if pr is None else out
 

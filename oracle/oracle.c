@@ -127,8 +127,24 @@ int oracle_expected_slots(int num_seqs, const int32_t *q_start,
 /* ------------------------------------------------------------------------ */
 typedef struct {
     int num_kv_heads, head_dim, block_size, num_blocks;
-    const uint16_t *k_pool, *v_pool;
+    const uint16_t *k_pool, *v_pool;  /* bf16 pools, or NULL with ... */
+    const uint8_t *k8, *v8;           /* ... fp8 e4m3 code pools and */
+    const float *k_scale, *v_scale;   /* one scale per KV head */
 } pool_view;
+
+static double e4m3_to_double(uint8_t c);
+
+/* Element e of row (blk, g, off) of the K (which = 0) or V pool, as a double:
+ * a bf16 value, or an fp8 code times its KV head's scale. */
+static double pool_elem(const pool_view *pv, int which, size_t row, int g, int e) {
+    const size_t at = row * (size_t)pv->head_dim + (size_t)e;
+    if (pv->k8) {
+        const uint8_t *p8 = which ? pv->v8 : pv->k8;
+        const float *sc = which ? pv->v_scale : pv->k_scale;
+        return e4m3_to_double(p8[at]) * (double)sc[g];
+    }
+    return bf16_to_double((which ? pv->v_pool : pv->k_pool)[at]);
+}
 
 static int attend_paged(const pool_view *pv, const double *q, int L,
                         const int32_t *bt_row, int g, double scale,
@@ -140,9 +156,9 @@ static int attend_paged(const pool_view *pv, const double *q, int L,
     for (int j = 0; j < L; ++j) {
         int32_t blk = bt_row[j / B];
         if (blk < 0 || blk >= pv->num_blocks) return OR_ERR_BLOCK_RANGE;
-        const uint16_t *kr = pv->k_pool + (size_t)(((long long)blk * H + g) * B + j % B) * d;
+        const size_t krow = (size_t)(((long long)blk * H + g) * B + j % B);
         double dot = 0.0;
-        for (int e = 0; e < d; ++e) dot += q[e] * bf16_to_double(kr[e]);
+        for (int e = 0; e < d; ++e) dot += q[e] * pool_elem(pv, 0, krow, g, e);
         x[j] = scale * dot;
         if (x[j] > M) M = x[j];
     }
@@ -154,8 +170,8 @@ static int attend_paged(const pool_view *pv, const double *q, int L,
     }
     for (int j = 0; j < L; ++j) {
         int32_t blk = bt_row[j / B];
-        const uint16_t *vr = pv->v_pool + (size_t)(((long long)blk * H + g) * B + j % B) * d;
-        for (int e = 0; e < d; ++e) out[e] += x[j] * bf16_to_double(vr[e]);
+        const size_t vrow = (size_t)(((long long)blk * H + g) * B + j % B);
+        for (int e = 0; e < d; ++e) out[e] += x[j] * pool_elem(pv, 1, vrow, g, e);
     }
     for (int e = 0; e < d; ++e) out[e] /= Z;
     return OR_OK;
@@ -299,6 +315,7 @@ int oracle_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     dc.pv.num_kv_heads = num_kv_heads; dc.pv.head_dim = head_dim;
     dc.pv.block_size = block_size; dc.pv.num_blocks = num_blocks;
     dc.pv.k_pool = k_pool; dc.pv.v_pool = v_pool;
+    dc.pv.k8 = dc.pv.v8 = NULL; dc.pv.k_scale = dc.pv.v_scale = NULL;
     dc.Hq = num_q_heads; dc.G = num_q_heads / num_kv_heads;
     dc.max_blocks = max_blocks_per_seq;
     dc.scale = effective_scale(scale, head_dim);
@@ -388,6 +405,7 @@ int oracle_prefill(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
     pc.pv.num_kv_heads = num_kv_heads; pc.pv.head_dim = head_dim;
     pc.pv.block_size = block_size; pc.pv.num_blocks = num_blocks;
     pc.pv.k_pool = k; pc.pv.v_pool = v;
+    pc.pv.k8 = pc.pv.v8 = NULL; pc.pv.k_scale = pc.pv.v_scale = NULL;
     pc.k = k; pc.v = v; pc.paged = paged;
     pc.Hq = num_q_heads; pc.G = num_q_heads / num_kv_heads;
     pc.num_seqs = num_seqs; pc.max_blocks = max_blocks_per_seq;
@@ -465,4 +483,114 @@ int oracle_to_bf16(long long n, const double *x, uint16_t *out) {
         out[j] = (uint16_t)(sign | ((bits >> 16) & 0x7fffu));
     }
     return OR_OK;
+}
+
+/*
+ * fp8 KV cache (e4m3, one scale per KV head and for K and V apart).  The
+ * pages compile flashinfer with FP8 off and name quantisation only as a
+ * serving option; the plainest reading of an "fp8 e4m3 cache with a per-head
+ * scale": a value x of KV head h is stored as the e4m3 code of x / scale[h]
+ * (the quotient in float, as the library computes it, then rounded to
+ * nearest-even in e4m3 with saturation at +-448) and read back as
+ * e4m3(code) * scale[h].
+ *
+ * e4m3 (OCP FP8, "fn" variant): 1 sign, 4 exponent bits (bias 7), 3
+ * significand bits; no infinities; S.1111.111 is NaN; largest finite 448;
+ * subnormals m * 2^-9.
+ */
+static double e4m3_to_double(uint8_t c) {
+    const int sg = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sg ? -v : v;
+}
+
+static uint8_t e4m3_from_double(double x) {
+    if (isnan(x)) return 0x7f;
+    const uint8_t sg = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs(x);
+    if (a >= 448.0) return sg | 0x7e;        /* saturate */
+    if (a < ldexp(1.0, -6)) {                 /* subnormal range: quantum 2^-9 */
+        const double m = nearbyint(ldexp(a, 9));  /* 0..8; 8 is the smallest normal */
+        return sg | (uint8_t)m;
+    }
+    int ex;
+    (void)frexp(a, &ex);                      /* a in [2^(ex-1), 2^ex) */
+    const int e = ex - 1;                     /* unbiased exponent */
+    double q = nearbyint(ldexp(a, 3 - e));    /* significand in eighths: 8..16 */
+    int eb = e + 7;
+    if (q >= 16.0) { q = 8.0; ++eb; }
+    const int code = (eb << 3) | ((int)q - 8);
+    return sg | (uint8_t)(code > 0x7e ? 0x7e : code);
+}
+
+int oracle_e4m3_from_float(long long n, const float *x, uint8_t *out) {
+    for (long long j = 0; j < n; ++j) out[j] = e4m3_from_double((double)x[j]);
+    return OR_OK;
+}
+
+int oracle_e4m3_to_double(long long n, const uint8_t *c, double *out) {
+    for (long long j = 0; j < n; ++j) out[j] = e4m3_to_double(c[j]);
+    return OR_OK;
+}
+
+/* Append with quantisation: for token i with slot >= 0, element e of KV head
+ * h goes to [slot / B][h][slot % B][e] as e4m3(float(x) / scale[h]).  The
+ * same checks as oracle_kv_append (slot range, duplicates). */
+int oracle_kv_append_fp8(int num_tokens, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         const uint16_t *k_new, const uint16_t *v_new, const int32_t *slot_mapping,
+                         const float *k_scale, const float *v_scale, uint8_t *k_pool, uint8_t *v_pool) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return OR_ERR_ARG;
+    const long long num_slots = (long long)num_blocks * block_size;
+    char *seen = calloc((size_t)num_slots, 1);
+    if (!seen) return OR_ERR_NOMEM;
+    for (int i = 0; i < num_tokens; ++i) {
+        const int32_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if ((long long)slot >= num_slots) { free(seen); return OR_ERR_SLOT_RANGE; }
+        if (seen[slot]) { free(seen); return OR_ERR_SLOT_DUP; }
+        seen[slot] = 1;
+        const long long blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const size_t src = ((size_t)i * num_kv_heads + h) * head_dim;
+            const size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off) * head_dim);
+            for (int e = 0; e < head_dim; ++e) {
+                const float kq = (float)bf16_to_double(k_new[src + e]) / k_scale[h];
+                const float vq = (float)bf16_to_double(v_new[src + e]) / v_scale[h];
+                k_pool[dst + e] = e4m3_from_double((double)kq);
+                v_pool[dst + e] = e4m3_from_double((double)vq);
+            }
+        }
+    }
+    free(seen);
+    return OR_OK;
+}
+
+/* Decode over fp8 pools: oracle_decode with every key and value element read
+ * as e4m3(code) * scale of its KV head. */
+int oracle_decode_fp8(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, double scale, const uint16_t *q, const uint8_t *k_pool,
+                      const uint8_t *v_pool, const float *k_scale, const float *v_scale,
+                      const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens,
+                      const int32_t *pairs, int num_pairs, double *out, int nthreads) {
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return OR_ERR_ARG;
+    int max_len = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (seq_lens[s] < 0) return OR_ERR_ARG;
+        if (seq_lens[s] > (long long)max_blocks_per_seq * block_size) return OR_ERR_BLOCK_RANGE;
+        if (seq_lens[s] > max_len) max_len = seq_lens[s];
+    }
+    decode_ctx dc;
+    dc.pv.num_kv_heads = num_kv_heads; dc.pv.head_dim = head_dim;
+    dc.pv.block_size = block_size; dc.pv.num_blocks = num_blocks;
+    dc.pv.k_pool = dc.pv.v_pool = NULL;
+    dc.pv.k8 = k_pool; dc.pv.v8 = v_pool; dc.pv.k_scale = k_scale; dc.pv.v_scale = v_scale;
+    dc.Hq = num_q_heads; dc.G = num_q_heads / num_kv_heads;
+    dc.max_blocks = max_blocks_per_seq;
+    dc.scale = effective_scale(scale, head_dim);
+    dc.q = q; dc.block_table = block_table; dc.seq_lens = seq_lens;
+    dc.pairs = pairs; dc.out = out;
+    long long n = pairs ? num_pairs : (long long)num_seqs * num_q_heads;
+    return run_items(decode_item, &dc, n, nthreads, (size_t)max_len + 1, head_dim);
 }

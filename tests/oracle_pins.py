@@ -476,6 +476,75 @@ def pin_rope_append_pool():
         assert np.array_equal(vp2[sl // 4, :, sl % 4], v[i])
 
 
+# ---------------------------------------------------------------------------
+# fp8 (e4m3) KV cache: one scale per KV head
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_codes_match_torch():
+    """Every e4m3 code decodes as torch's float8_e4m3fn does; float32 values
+    in range encode as torch rounds them (nearest, ties to even); beyond 448
+    the code saturates."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_double(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+    g = torch.Generator().manual_seed(8)
+    x = torch.cat([(torch.randn(20000, generator=g) * 40).clamp(-447, 447),
+                   torch.randn(2000, generator=g) * 1e-3])
+    assert np.array_equal(oracle.e4m3_from_float(x.numpy()), x.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    assert list(oracle.e4m3_from_float(np.array([1e4, -1e4, 449.0], np.float32))) == [0x7e, 0xfe, 0x7e]
+
+
+def _fp8_case(seed):
+    shape = wl.Shape(num_q_heads=8, num_kv_heads=2, head_dim=16, block_size=4, num_blocks=12)
+    g = torch.Generator().manual_seed(seed)
+    alloc = wl.BlockAllocator(shape.num_blocks, shape.block_size,
+                              torch.randperm(shape.num_blocks, generator=g).tolist())
+    st = wl.make_step(alloc, shape, [0, 1], [21, 9], [21, 9], 0, g)
+    ks = np.array([0.05, 0.02], np.float32)
+    vs = np.array([0.03, 0.07], np.float32)
+    kp0 = np.random.default_rng(seed).integers(0, 126, size=(12, 2, 4, 16)).astype(np.uint8)
+    vp0 = np.random.default_rng(seed + 1).integers(0, 126, size=(12, 2, 4, 16)).astype(np.uint8)
+    return shape, st, ks, vs, kp0, vp0
+
+
+def pin_kv_append_fp8_codes():
+    """A key element x of KV head h lands as the e4m3 code of float(x) / scale[h]
+    (torch's float32 division and float8 cast); untouched bytes keep theirs."""
+    shape, st, ks, vs, kp0, vp0 = _fp8_case(12)
+    kp, vp = oracle.kv_append_fp8(bits(st.k_new), bits(st.v_new), st.slot_mapping, ks, vs, kp0, vp0)
+    kq = (st.k_new.float() / torch.from_numpy(ks)[None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    vq = (st.v_new.float() / torch.from_numpy(vs)[None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    touched = np.zeros(kp.shape[0] * 4, dtype=bool)
+    for i, sl in enumerate(st.slot_mapping):
+        assert np.array_equal(kp[sl // 4, :, sl % 4], kq[i]) and np.array_equal(vp[sl // 4, :, sl % 4], vq[i])
+        touched[sl] = True
+    keep = ~np.repeat(touched.reshape(-1, 4)[:, None, :, None], 2, axis=1).repeat(16, axis=3)
+    assert np.array_equal(kp[keep], kp0[keep]) and np.array_equal(vp[keep], vp0[keep])
+
+
+def pin_decode_fp8_vs_sdpa():
+    """Decode over fp8 pools equals torch's float64 SDPA over the dequantized
+    keys and values (code * scale), gathered in token order."""
+    shape, st, ks, vs, kp0, vp0 = _fp8_case(13)
+    kp, vp = oracle.kv_append_fp8(bits(st.k_new), bits(st.v_new), st.slot_mapping, ks, vs, kp0, vp0)
+    g = torch.Generator().manual_seed(14)
+    q = wl.bf16_randn((2, 8, 16), g)
+    lens = np.array([21, 9], np.int32)
+    out = oracle.decode_fp8(bits(q), kp, vp, ks, vs, st.block_table, lens)
+    deq = lambda pool, sc: torch.from_numpy(pool).view(torch.float8_e4m3fn).double() * torch.from_numpy(sc).double()[None, :, None, None]
+    kd, vd = deq(kp, ks), deq(vp, vs)
+    for s_, L in enumerate(lens):
+        idx = [(int(st.block_table[s_, j // 4]), j % 4) for j in range(L)]
+        K = torch.stack([kd[b, :, o] for b, o in idx])  # [L, Hkv, d]
+        V = torch.stack([vd[b, :, o] for b, o in idx])
+        Kx = K.repeat_interleave(4, dim=1).permute(1, 0, 2)
+        Vx = V.repeat_interleave(4, dim=1).permute(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(q[s_].double()[:, None, :], Kx, Vx)[:, 0, :]
+        np.testing.assert_allclose(out[s_], ref.numpy(), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_decode_vs_sdpa, pin_prefill_dense_vs_sdpa, pin_prefill_paged_vs_sdpa,
     pin_chunked_prefill_vs_sdpa, pin_append_layout, pin_append_errors,
@@ -485,4 +554,5 @@ ALL_PINS = [
     pin_mixed_step_composition, pin_copy_blocks_fork_vs_sdpa, pin_copy_blocks_swap_round_trip,
     pin_copy_blocks_errors, pin_rope_identity_at_position_zero, pin_rope_is_complex_rotation,
     pin_rope_relative_position, pin_to_bf16_rounding, pin_rope_append_pool,
+    pin_e4m3_codes_match_torch, pin_kv_append_fp8_codes, pin_decode_fp8_vs_sdpa,
 ]

@@ -35,6 +35,10 @@ MUTATIONS = [
     ("rope_interleaved_pairs", "x1 = bf16_to_double(x[base + i + half]);", "x1 = bf16_to_double(x[base + (i ^ 1)]);", 1),
     ("rope_frequency", "pow(theta, -2.0 * (double)i / (double)head_dim)", "pow(theta, -1.0 * (double)i / (double)head_dim)", 1),
     ("bf16_truncates", "nearbyint(ldexp(a, -qexp))", "floor(ldexp(a, -qexp))", 1),
+    ("e4m3_bias", "ldexp(8.0 + m, e - 10)", "ldexp(8.0 + m, e - 9)", 1),
+    ("e4m3_rounds_down", "double q = nearbyint(ldexp(a, 3 - e));", "double q = floor(ldexp(a, 3 - e));", 1),
+    ("fp8_scale_multiplied", "(float)bf16_to_double(k_new[src + e]) / k_scale[h];", "(float)bf16_to_double(k_new[src + e]) * k_scale[h];", 1),
+    ("fp8_read_scale_dropped", "return e4m3_to_double(p8[at]) * (double)sc[g];", "return e4m3_to_double(p8[at]);", 1),
 ]
 
 
