@@ -21,16 +21,16 @@ MUTATIONS = [
     ("causal_off_by_one", "int L = (int)(p0 + i + 1);", "int L = (int)(p0 + i);", 1),
     ("no_normalise", "for (int e = 0; e < d; ++e) out[e] /= Z;", "", 2),
     ("append_swaps_kv", "k_pool[dst + e] = k_new[src + e];", "k_pool[dst + e] = v_new[src + e];", 1),
-    ("v_read_from_k_pool", "const uint16_t *vr = pv->v_pool +", "const uint16_t *vr = pv->k_pool +", 1),
+    ("v_read_from_k_pool", "(which ? pv->v_pool : pv->k_pool)[at]", "(which ? pv->k_pool : pv->k_pool)[at]", 1),
     ("pool_layout_nhd", "size_t dst = (size_t)(((blk * num_kv_heads + h) * block_size + off) * head_dim);",
-     "size_t dst = (size_t)(((blk * block_size + off) * num_kv_heads + h) * head_dim);", 1),
-    ("block_offset_wrong", "const uint16_t *kr = pv->k_pool + (size_t)(((long long)blk * H + g) * B + j % B) * d;",
-     "const uint16_t *kr = pv->k_pool + (size_t)(((long long)blk * H + g) * B + (B - 1 - j % B)) * d;", 1),
+     "size_t dst = (size_t)(((blk * block_size + off) * num_kv_heads + h) * head_dim);", 2),
+    ("block_offset_wrong", "const size_t krow = (size_t)(((long long)blk * H + g) * B + j % B);",
+     "const size_t krow = (size_t)(((long long)blk * H + g) * B + (B - 1 - j % B));", 1),
     ("prefix_ignored", "int p0 = pc->prefix ? pc->prefix[s] : 0;", "int p0 = 0;", 1),
     ("default_scale_wrong", "1.0 / sqrt((double)head_dim)", "1.0 / (double)head_dim", 1),
     ("slot_formula_wrong", "slots_out[q_start[s] + i] = blk * block_size + p % block_size;",
      "slots_out[q_start[s] + i] = blk * block_size + p / block_size;", 1),
-    ("dup_check_dropped", "if (seen[slot]) { free(seen); return OR_ERR_SLOT_DUP; }", "", 1),
+    ("dup_check_dropped", "if (seen[slot]) { free(seen); return OR_ERR_SLOT_DUP; }", "", 2),
     ("rope_sign", "out[base + i] = x0 * c - x1 * s;", "out[base + i] = x0 * c + x1 * s;", 1),
     ("rope_interleaved_pairs", "x1 = bf16_to_double(x[base + i + half]);", "x1 = bf16_to_double(x[base + (i ^ 1)]);", 1),
     ("rope_frequency", "pow(theta, -2.0 * (double)i / (double)head_dim)", "pow(theta, -1.0 * (double)i / (double)head_dim)", 1),
