@@ -246,6 +246,7 @@ def run_ours(args, world, rank, local):
     prefill = measure_prefill(pa, wl, dev, bf16_peak, peak_src, args.prefill_iters) if rank == 0 else None
     copy = measure_copy(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
     rope = measure_rope(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
+    fp8 = measure_fp8_decode(pa, wl, dev, hbm_peak, max(20, min(args.steps, 500))) if rank == 0 else None
 
     clocks = clk.summary()
     traffic = load_traffic("decode_splitk", nbytes, st.num_seqs)
@@ -274,6 +275,7 @@ def run_ours(args, world, rank, local):
         "prefill": prefill,
         "block_copy": copy,
         "rope_append": rope,
+        "fp8_decode": fp8,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kp, vp, st, split, args.cpu_seconds)
@@ -499,6 +501,41 @@ def measure_rope(pa, wl, dev, hbm_peak, iters):
         res[name] = {"tokens": T, "ms": round(t * 1e3, 4), "GBps": round(nbytes / t / 1e9, 1),
                      "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 4)}
     return {"kernel": "rope_append_kernel", "l2": "flushed (256 MB write) before each launch", **res}
+
+
+def measure_fp8_decode(pa, wl, dev, hbm_peak, steps):
+    """The decode step's attention (Llama-7B shape, 128 sequences) over fp8
+    (e4m3) pools with per-KV-head scales: pa_decode_fp8.  Bytes counted: the
+    fp8 K/V (one byte per element), q, out, tables, lengths and split
+    partials; the rate in sequences decoded per second as well."""
+    shape, _, _, st = wl.llama7b_decode(pool_device=None)
+    N, H, B, d = shape.num_blocks, shape.num_kv_heads, shape.block_size, shape.head_dim
+    kp = torch.randint(0, 126, (N, H, B, d), dtype=torch.uint8, device=dev)
+    vp = torch.randint(0, 126, (N, H, B, d), dtype=torch.uint8, device=dev)
+    ks = torch.full((H,), 0.02, dtype=torch.float32, device=dev)
+    vs = torch.full((H,), 0.02, dtype=torch.float32, device=dev)
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
+    q, bt, lens = tod(st.q), tod(st.block_table), tod(st.seq_lens)
+    ws = pa.workspace(shape, st.num_seqs, st.max_seq_len, dev)
+    out = torch.empty_like(q)
+    for _ in range(5):
+        pa.decode_fp8(shape, q, kp, vp, ks, vs, bt, lens, st.max_seq_len, out=out, ws=ws)
+    pa.check_device_error()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        pa.decode_fp8(shape, q, kp, vp, ks, vs, bt, lens, st.max_seq_len, out=out, ws=ws)
+    b.record()
+    torch.cuda.synchronize(dev)
+    pa.check_device_error()
+    t = a.elapsed_time(b) / 1e3 / steps
+    split, _ = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
+    nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
+    fp8_bytes = nb["decode"] - nb["kv"] // 2
+    return {"kernel": "decode_splitk_kernel<128,16,*,fp8> + decode_merge_kernel", "ms": round(t * 1e3, 5),
+            "GBps": round(fp8_bytes / t / 1e9, 1), "frac_hbm": round(fp8_bytes / t / 1e9 / hbm_peak, 4),
+            "algorithmic_bytes": int(fp8_bytes), "sequences_per_s": round(st.num_seqs / t, 1),
+            "l2": "inputs larger than L2 (fp8 pools 1.2 GB)"}
 
 
 # ------------------------------------------------------------ CPU oracle --

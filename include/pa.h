@@ -202,6 +202,30 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
                       int num_seqs, int max_seq_len, void *out, void *stream);
 
 /*
+ * fp8 KV cache: pools of e4m3 codes (OCP FP8 "e4m3fn": 1 sign, 4 exponent
+ * bits with bias 7, 3 significand bits, largest finite 448, no infinities),
+ * same [N][Hkv][B][d] layout with one byte per element, and one float scale
+ * per KV head for K and one for V (device arrays [Hkv]): a value x of KV head
+ * h is stored as the code of x / scale[h] (float division, nearest even,
+ * saturating at +-448) and read as code * scale[h].  The pages name fp8 only
+ * as a serving option (flashinfer's FP8 switch; a quantize flag), so this is
+ * the plainest reading of an fp8 cache with per-head scales.
+ *
+ * pa_kv_append_fp8: pa_kv_append into fp8 pools (same slot rules and error
+ * behaviour).
+ * pa_decode_fp8: pa_decode over fp8 pools (head_dim 128 only, else
+ * PA_ERR_UNSUPPORTED); same workspace (pa_workspace_size), split-K plan,
+ * errors and asynchrony.  q and out stay bf16.
+ */
+int pa_kv_append_fp8(const pa_shape_t *shape, const void *k_new, const void *v_new,
+                     const int32_t *slot_mapping, int num_tokens, const float *k_scale,
+                     const float *v_scale, void *k_pool, void *v_pool, void *stream);
+int pa_decode_fp8(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
+                  const float *k_scale, const float *v_scale, const int32_t *block_table,
+                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                  void *out, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Rotary position embedding of a step's new tokens, fused with their KV
  * append (the position-encoding mode the pages' flashinfer build compiles in,
  * Blitzscale docs, section "Build"; the rotation of RoFormer with the Llama /

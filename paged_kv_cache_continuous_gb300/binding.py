@@ -29,7 +29,7 @@ ERR_TIMEOUT = 7
 EXPORTS = [
     "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode",
     "pa_decode_noalloc", "pa_prefill",
-    "pa_mixed_step", "pa_copy_blocks", "pa_rope_append", "pa_set_validation", "pa_check_device_error", "pa_last_error",
+    "pa_mixed_step", "pa_copy_blocks", "pa_rope_append", "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_validation", "pa_check_device_error", "pa_last_error",
     "pa_set_decode_split",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
     "pa_alloc_num_free", "pa_alloc_num_blocks_of", "pa_alloc_block_table",
@@ -78,6 +78,8 @@ def load():
         "pa_mixed_step": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P], I),
         "pa_copy_blocks": ([SP, P, P, I, P, P, I, P, P, I, P], I),
         "pa_rope_append": ([SP, P, P, P, P, P, I, ctypes.c_float, P, P, P, P], I),
+        "pa_kv_append_fp8": ([SP, P, P, P, I, P, P, P, P, P], I),
+        "pa_decode_fp8": ([SP, P, P, P, P, P, P, I, P, I, I, P, P, S, P], I),
         "pa_set_validation": ([I], I),
         "pa_check_device_error": ([P], I),
         "pa_last_error": ([], ctypes.c_char_p),
@@ -195,6 +197,43 @@ def rope_append(shape, q, k_new, v_new, positions, slot_mapping, k_pool, v_pool,
                                  _i32(slot_mapping, "slot_mapping"), T, float(theta), _bf16(q_out, "q_out"),
                                  _bf16(k_pool, "k_pool"), _bf16(v_pool, "v_pool"), _stream(stream)))
     return q_out
+
+
+def _u8(t: torch.Tensor, name: str):
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{name} must be uint8 (e4m3 codes)")
+    return _ptr(t)
+
+
+def _f32(t: torch.Tensor, name: str):
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return _ptr(t)
+
+
+def kv_append_fp8(shape, k_new, v_new, slot_mapping, k_scale, v_scale, k_pool, v_pool, stream=None):
+    """pa_kv_append_fp8: quantising append into uint8 (e4m3 code) pools."""
+    T = int(slot_mapping.shape[0])
+    _check(load().pa_kv_append_fp8(ctypes.byref(_shape(shape)), _bf16(k_new, "k_new"), _bf16(v_new, "v_new"),
+                                   _i32(slot_mapping, "slot_mapping"), T, _f32(k_scale, "k_scale"),
+                                   _f32(v_scale, "v_scale"), _u8(k_pool, "k_pool"), _u8(v_pool, "v_pool"),
+                                   _stream(stream)))
+
+
+def decode_fp8(shape, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, max_seq_len: int, out=None,
+               ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_decode_fp8: decode over uint8 (e4m3 code) pools with per-KV-head scales."""
+    S = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(shape, S, max_seq_len, q.device)
+    _check(load().pa_decode_fp8(ctypes.byref(_shape(shape)), _bf16(q, "q"), _u8(k_pool, "k_pool"),
+                                _u8(v_pool, "v_pool"), _f32(k_scale, "k_scale"), _f32(v_scale, "v_scale"),
+                                _i32(block_table, "block_table"), int(block_table.shape[1]),
+                                _i32(seq_lens, "seq_lens"), S, int(max_seq_len), _bf16(out, "out"), _ptr(ws),
+                                ws.numel(), _stream(stream)))
+    return out
 
 
 def decode(shape, q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, out=None,

@@ -38,34 +38,40 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
-template <int D, int BS>
+// FP8: the pools hold e4m3 codes (one byte per element) with one scale per KV
+// head for K and for V.
+template <int D, int BS, bool FP8 = false>
 struct DecodeCfg {
-    static constexpr int kHalves = D / 64;                 // 64-column TMA boxes per row
+    static constexpr int kEB = FP8 ? 1 : 2;                // bytes per pool element
+    static constexpr int kBoxCols = 128 / kEB;             // elements per 128-byte TMA box row
+    static constexpr int kHalves = D / kBoxCols;           // TMA boxes per row
     static constexpr int kHalfBytes = BS * 128;            // one box: BS rows x 128 B
     static constexpr int kKVBytes = kHalves * kHalfBytes;  // K (or V) of one block
     static constexpr int kStageBytes = 2 * kKVBytes;
-    static constexpr int kStages = (BS == 16) ? 8 : 4;     // multiple of kConsumerWarps
+    // multiple of kConsumerWarps; fp8 stages are half the bytes, so twice as
+    // many keep the same bytes in flight
+    static constexpr int kStages = ((BS == 16) ? 8 : 4) * (FP8 ? 2 : 1);
     static constexpr int kKSteps = D / 16;                 // QK^T k-steps
     static constexpr int kNTiles = D / 8;                  // PV n-tiles
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kSmemBytes = kRingBytes + 2 * kStages * 8 + 16 + 1024;
-    static_assert(kConsumerWarps * 16 * D * 4 + kConsumerWarps * 16 * 8 <= kRingBytes,
-                  "merge scratch must fit in the ring");
+    static constexpr int kScratchBytes = kConsumerWarps * 16 * D * 4 + kConsumerWarps * 16 * 8;
+    static constexpr int kRegionBytes = kRingBytes > kScratchBytes ? kRingBytes : kScratchBytes;
+    static constexpr int kSmemBytes = kRegionBytes + 2 * kStages * 8 + 16 + 1024;
 };
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-template <int D, int BS, bool BIG_G>
+template <int D, int BS, bool BIG_G, bool FP8>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-    using C = DecodeCfg<D, BS>;
+    using C = DecodeCfg<D, BS, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kRingBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kRegionBytes);
     uint64_t *empty = full + C::kStages;
     int *s_abort = reinterpret_cast<int *>(empty + C::kStages);
 
@@ -102,45 +108,40 @@ __global__ void __launch_bounds__(kThreads, 3)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
-        int issued = 0;
-        bool ok = true;
-        for (int base = 0; base < nblk && ok; base += 32) {
-            const int idx = base + lane;
-            int32_t blk = idx < nblk ? bt[idx] : 0;
-            if (idx < nblk && (unsigned)blk >= (unsigned)a.num_blocks) {
-                set_error(a.err, PA_ERR_BAD_INDEX);
-                blk = 0;  // never dereference an out-of-range block
-            }
-            const int cnt = min(32, nblk - base);
-            for (int j = 0; j < cnt; ++j) {
-                const int bj = __shfl_sync(0xffffffffu, blk, j);
-                const int i = base + j;
-                if (lane == 0 && ok) {
-                    const int st = i % C::kStages;
-                    if (i >= C::kStages && !mbar_wait(&empty[st], ((i / C::kStages) - 1) & 1, a.err)) {
-                        ok = false;
-                        atomicExch(s_abort, 1);
-                    } else {
-                        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-                        uint8_t *sk = smem + st * C::kStageBytes;
-                        uint8_t *sv = sk + C::kKVBytes;
-                        const int row = (bj * a.num_kv_heads + g) * BS;
-#pragma unroll
-                        for (int hf = 0; hf < C::kHalves; ++hf) {
-                            tma_load_2d(sk + hf * C::kHalfBytes, &tm_k, &full[st], hf * 64, row);
-                            tma_load_2d(sv + hf * C::kHalfBytes, &tm_v, &full[st], hf * 64, row);
-                        }
-                        issued = i + 1;
-                    }
+        // One lane per stage: lane l fills stage l with blocks l, l + kStages,
+        // ..., each as soon as the consumers have freed it, independently of
+        // the other lanes, so the TMA issue of a block overlaps its neighbours'.
+        constexpr int kLanes = C::kStages;
+        static_assert(kLanes <= 32, "one producer lane per stage");
+        int last = -1;  // the last block this lane issued (into stage `lane`)
+        bool good = true;
+        if (lane < kLanes) {
+            for (int i = lane; i < nblk; i += kLanes) {
+                int32_t blk = bt[i];
+                if ((unsigned)blk >= (unsigned)a.num_blocks) {
+                    set_error(a.err, PA_ERR_BAD_INDEX);
+                    blk = 0;  // never dereference an out-of-range block
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (i >= C::kStages && !mbar_wait(&empty[lane], ((i / C::kStages) - 1) & 1, a.err)) {
+                    good = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[lane], C::kStageBytes);
+                last = i;
+                uint8_t *sk = smem + lane * C::kStageBytes;
+                uint8_t *sv = sk + C::kKVBytes;
+                const int row = (blk * a.num_kv_heads + g) * BS;
+#pragma unroll
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    tma_load_2d(sk + hf * C::kHalfBytes, &tm_k, &full[lane], hf * C::kBoxCols, row);
+                    tma_load_2d(sv + hf * C::kHalfBytes, &tm_v, &full[lane], hf * C::kBoxCols, row);
+                }
             }
         }
-        // Drain: every copy this CTA issued has landed before it may exit.
-        if (lane == 0) {
-            for (int i = max(0, issued - C::kStages); i < issued; ++i)
-                mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1, a.err);
-        }
+        if (!__all_sync(0xffffffffu, good) && lane == 0) atomicExch(s_abort, 1);
+        // Drain: every copy this CTA issued has landed before it may exit (a
+        // stage's earlier blocks were consumed before it was refilled).
+        if (last >= 0) mbar_wait(&full[lane], (last / C::kStages) & 1, a.err);
         return;
     }
 
@@ -151,6 +152,23 @@ __global__ void __launch_bounds__(kThreads, 3)
     const __nv_bfloat16 *qg = a.q + ((size_t)s * a.num_q_heads + (size_t)g * G) * D;
 
     uint32_t qa[C::kKSteps][4];
+    if (FP8) {
+        // fp16 A fragments with the k-step's 16 columns permuted to match the
+        // byte order ldmatrix gives the fp8 keys: MMA columns 2c, 2c+1 hold
+        // d = 4c, 4c+1 and columns 2c+8, 2c+9 hold d = 4c+2, 4c+3 (c = lane % 4).
+        const int c4 = (lane & 3) * 4;
+        auto qf = [&](int row, int col) {
+            return row < G ? pack_f16x2(__bfloat162float(qg[row * D + col]), __bfloat162float(qg[row * D + col + 1]))
+                           : 0u;
+        };
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+            qa[ks][0] = qf(r0, ks * 16 + c4);
+            qa[ks][2] = qf(r0, ks * 16 + c4 + 2);
+            qa[ks][1] = BIG_G ? qf(r0 + 8, ks * 16 + c4) : 0u;
+            qa[ks][3] = BIG_G ? qf(r0 + 8, ks * 16 + c4 + 2) : 0u;
+        }
+    } else
 #pragma unroll
     for (int ks = 0; ks < C::kKSteps; ++ks) {
         qa[ks][0] = r0 < G ? ld_u32(qg + r0 * D + ks * 16 + cq) : 0u;
@@ -169,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int nt = 0; nt < C::kNTiles; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};  // rows r0, r0 + 8 (log2 units)
     float l_run[2] = {0.f, 0.f};              // this lane's share of the row sums
-    const float sl = a.scale_log2;
+    const float sl = FP8 ? a.scale_log2 * a.k_scale[g] : a.scale_log2;
 
     for (int i = warp; i < nblk; i += kConsumerWarps) {
         const int st = i % C::kStages;
@@ -198,7 +216,28 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (sb * 16 >= valid) break;
             // ---- S = Q K^T over 16 keys (two n-tiles of 8 keys)
             float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
+            if (FP8) {
+                // one 16-byte chunk of a key row is one k-step; matrices: keys
+                // 0-7 / 8-15 x k-steps 2kp, 2kp+1.  A lane's 4 bytes are d = 4c..4c+3.
+                const int mat = lane >> 3;
+                const int t = sb * 16 + (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+                for (int kp = 0; kp < C::kKSteps / 2; ++kp) {
+                    const int jj = 2 * kp + (mat & 1);
+                    const uint32_t addr = sk + t * 128 + (((jj ^ (t & 7))) << 4);
+                    uint32_t b00, b01, b10, b11;  // (keys 0-7, ks), (0-7, ks+1), (8-15, ks), (8-15, ks+1)
+                    ldmatrix_x4(addr, b00, b01, b10, b11);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int ks = 2 * kp + u;
+                        const uint32_t lo = u ? b01 : b00, hi = u ? b11 : b10;
+                        mma_f16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(lo),
+                                      e4m3x2_to_f16x2(lo >> 16));
+                        mma_f16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(hi),
+                                      e4m3x2_to_f16x2(hi >> 16));
+                    }
+                }
+            } else {
                 const int mat = lane >> 3;
                 const int t = sb * 16 + (lane & 7) + ((mat >> 1) << 3);
 #pragma unroll
@@ -247,16 +286,44 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (!BIG_G) {
                 p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
             }
-            const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]);
-            const uint32_t pa1 = pack_bf16x2(p[0][2], p[0][3]);
-            const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]);
-            const uint32_t pa3 = pack_bf16x2(p[1][2], p[1][3]);
-            // The row sums use the same bf16-rounded weights that multiply V,
-            // so the output is an exact convex combination of the values.
-            l_run[0] = l_run[0] * alpha[0] + (bf16x2_sum(pa0) + bf16x2_sum(pa2));
-            if (BIG_G) l_run[1] = l_run[1] * alpha[1] + (bf16x2_sum(pa1) + bf16x2_sum(pa3));
+            auto pk = [&](float lo, float hi) { return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
+            auto psum = [&](uint32_t v) { return FP8 ? f16x2_sum(v) : bf16x2_sum(v); };
+            const uint32_t pa0 = pk(p[0][0], p[0][1]);
+            const uint32_t pa1 = pk(p[0][2], p[0][3]);
+            const uint32_t pa2 = pk(p[1][0], p[1][1]);
+            const uint32_t pa3 = pk(p[1][2], p[1][3]);
+            // The row sums use the same rounded weights that multiply V, so the
+            // output is an exact convex combination of the values.
+            l_run[0] = l_run[0] * alpha[0] + (psum(pa0) + psum(pa2));
+            if (BIG_G) l_run[1] = l_run[1] * alpha[1] + (psum(pa1) + psum(pa3));
             // ---- acc += P V over the same 16 keys
-            {
+            if (FP8) {
+                // matrices: keys 0-7 / 8-15 x 16-byte d chunks 2jp, 2jp+1,
+                // transposed: a lane holds, per matrix, keys 2c, 2c+1 x d = 2n, 2n+1
+                // of the chunk (n = lane / 4).  Even d go to one n-tile, odd d
+                // to the next: acc[4 jp + 2 u + par] column 2c + e is
+                // d = 16 (2 jp + u) + 4c + 2e + par.
+                const int mat = lane >> 3;
+                const int t = sb * 16 + (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+                for (int jp = 0; jp < D / 32; ++jp) {
+                    const int jj = 2 * jp + (mat >> 1);
+                    const uint32_t addr = sv + t * 128 + (((jj ^ (t & 7))) << 4);
+                    uint32_t v0, v1, v2, v3;  // (keys 0-7, chunk 2jp), (8-15, 2jp), (0-7, 2jp+1), (8-15, 2jp+1)
+                    ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t lo = u ? v2 : v0, hi = u ? v3 : v1;
+#pragma unroll
+                        for (int par = 0; par < 2; ++par) {
+                            const uint32_t sel = par ? 0x3131u : 0x2020u;  // bytes (1, 3) or (0, 2)
+                            mma_f16_16816(acc[4 * jp + 2 * u + par], pa0, pa1, pa2, pa3,
+                                          e4m3x2_to_f16x2(__byte_perm(lo, 0u, sel)),
+                                          e4m3x2_to_f16x2(__byte_perm(hi, 0u, sel)));
+                        }
+                    }
+                }
+            } else {
                 const int mat = lane >> 3;
                 const int t = sb * 16 + (lane & 7) + ((mat & 1) << 3);
 #pragma unroll
@@ -281,6 +348,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
         l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
     }
+    if (FP8) {
+        const float vs = a.v_scale[g];
+#pragma unroll
+        for (int nt = 0; nt < C::kNTiles; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] *= vs;
+    }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     float *red_acc = reinterpret_cast<float *>(smem);                       // [W][16][D]
     float *red_ml = red_acc + kConsumerWarps * 16 * D;                      // [W][16][2]
@@ -289,9 +363,15 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int row = r0 + rr * 8;
         float *dst = red_acc + (warp * 16 + row) * D;
 #pragma unroll
-        for (int nt = 0; nt < C::kNTiles; ++nt)
-            *reinterpret_cast<float2 *>(dst + nt * 8 + cq) =
-                make_float2(acc[nt][rr * 2 + 0], acc[nt][rr * 2 + 1]);
+        for (int nt = 0; nt < C::kNTiles; ++nt) {
+            if (FP8) {
+                const int d0 = 16 * (nt >> 1) + 4 * (lane & 3) + (nt & 1);
+                dst[d0] = acc[nt][rr * 2 + 0];
+                dst[d0 + 2] = acc[nt][rr * 2 + 1];
+            } else {
+                *reinterpret_cast<float2 *>(dst + nt * 8 + cq) = make_float2(acc[nt][rr * 2 + 0], acc[nt][rr * 2 + 1]);
+            }
+        }
         if ((lane & 3) == 0) {
             red_ml[(warp * 16 + row) * 2 + 0] = m_run[rr];
             red_ml[(warp * 16 + row) * 2 + 1] = l_run[rr];
@@ -377,20 +457,20 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
         *reinterpret_cast<__nv_bfloat162 *>(o + e) = __floats2bfloat162_rn(accv[e] * inv, accv[e + 1] * inv);
 }
 
-template <int D, int BS, bool BIG_G>
+template <int D, int BS, bool BIG_G, bool FP8>
 cudaError_t launch_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                             cudaStream_t stream) {
-    using C = DecodeCfg<D, BS>;
+    using C = DecodeCfg<D, BS, FP8>;
     static bool attr_set = false;  // benign race: the attribute call is idempotent
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitk_kernel<D, BS, BIG_G>,
+        cudaError_t e = cudaFuncSetAttribute(decode_splitk_kernel<D, BS, BIG_G, FP8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-    decode_splitk_kernel<D, BS, BIG_G><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_k, tm_v, a);
+    decode_splitk_kernel<D, BS, BIG_G, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_k, tm_v, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.max_splits <= 1) return e;
     dim3 mgrid((a.num_q_heads + 3) / 4, a.num_seqs);
@@ -424,16 +504,18 @@ size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int m
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, int block_size, cudaStream_t stream) {
+                          int head_dim, int block_size, cudaStream_t stream, bool fp8) {
     const bool big = a.group > 8;
-#define PA_DEC(D, BS)                                                                  \
-    if (head_dim == D && block_size == BS)                                             \
-        return big ? launch_decode_t<D, BS, true>(tm_k, tm_v, a, stream)               \
-                   : launch_decode_t<D, BS, false>(tm_k, tm_v, a, stream);
-    PA_DEC(128, 16)
-    PA_DEC(128, 32)
-    PA_DEC(64, 16)
-    PA_DEC(64, 32)
+#define PA_DEC(D, BS, F8)                                                              \
+    if (head_dim == D && block_size == BS && fp8 == F8)                                \
+        return big ? launch_decode_t<D, BS, true, F8>(tm_k, tm_v, a, stream)           \
+                   : launch_decode_t<D, BS, false, F8>(tm_k, tm_v, a, stream);
+    PA_DEC(128, 16, false)
+    PA_DEC(128, 32, false)
+    PA_DEC(64, 16, false)
+    PA_DEC(64, 32, false)
+    PA_DEC(128, 16, true)
+    PA_DEC(128, 32, true)
 #undef PA_DEC
     return cudaErrorInvalidValue;
 }

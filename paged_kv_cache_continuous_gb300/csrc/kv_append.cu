@@ -42,6 +42,52 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// fp8 cache: element e of KV head h is stored as the e4m3 code of
+// x / scale[h] (IEEE float division, then nearest-even with saturation at
+// +-448).  One thread per 16 codes (32 bytes of bf16 in, 16 bytes out).
+__global__ void __launch_bounds__(256)
+    kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                         const int32_t *__restrict__ slot_mapping, long long num_vec, int vec_per_row,
+                         int num_kv_heads, int block_size, long long num_slots, const float *__restrict__ k_scale,
+                         const float *__restrict__ v_scale, uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
+                         int *err, int check_err_first) {
+    if (check_err_first && *(volatile int *)err != 0) return;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < num_vec; idx += stride) {
+        const int j = (int)(idx % vec_per_row);  // 16-code piece within the row
+        const long long th = idx / vec_per_row;  // token * Hkv + head
+        const int h = (int)(th % num_kv_heads);
+        const long long tok = th / num_kv_heads;
+        const int slot = __ldg(slot_mapping + tok);
+        if (slot < 0) continue;
+        if ((long long)slot >= num_slots) {
+            set_error(err, PA_ERR_BAD_INDEX);
+            continue;
+        }
+        const long long blk = slot / block_size, off = slot % block_size;
+        const long long dst = ((blk * num_kv_heads + h) * block_size + off) * vec_per_row + j;
+        const float ks = __ldg(k_scale + h), vs = __ldg(v_scale + h);
+        auto quant = [](const uint4 *src, long long at, float sc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint4 x = __ldg(src + 2 * at + q);
+                const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int k = 0; k < 4; k += 2) {
+                    const float2 a = bf16x2_unpack(in[k]), b = bf16x2_unpack(in[k + 1]);
+                    const uint32_t lo = f32x2_to_e4m3x2(a.x / sc, a.y / sc);
+                    const uint32_t hi = f32x2_to_e4m3x2(b.x / sc, b.y / sc);
+                    w[2 * q + k / 2] = lo | (hi << 16);
+                }
+            }
+            return make_uint4(w[0], w[1], w[2], w[3]);
+        };
+        k_pool[dst] = quant(k_new, idx, ks);
+        v_pool[dst] = quant(v_new, idx, vs);
+    }
+}
+
 // Validation mode: every index the kernels of one call will read is checked
 // here first; a bad one sets the error word (PA_ERR_BAD_INDEX) and the
 // call's other kernels, launched with check_err_first, return untouched.
@@ -106,6 +152,24 @@ cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_
     kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slot_mapping,
         num_vec, vec_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size,
+        reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool), err, check_err_first);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append_fp8(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
+                                 const int32_t *slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, const float *k_scale, const float *v_scale,
+                                 uint8_t *k_pool, uint8_t *v_pool, int *err, int check_err_first,
+                                 cudaStream_t stream) {
+    const int vec_per_row = head_dim / 16;  // 16 codes per output vector
+    const long long num_vec = (long long)num_tokens * num_kv_heads * vec_per_row;
+    if (num_vec == 0) return cudaSuccess;
+    const int threads = 256;
+    long long blocks = (num_vec + threads - 1) / threads;
+    if (blocks > 65535LL * 4) blocks = 65535LL * 4;
+    kv_append_fp8_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slot_mapping, num_vec,
+        vec_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size, k_scale, v_scale,
         reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool), err, check_err_first);
     return cudaGetLastError();
 }

@@ -131,6 +131,23 @@ int make_pool_map(CUtensorMap *m, const void *pool, const pa_shape_t *sh) {
     return PA_OK;
 }
 
+// fp8 pool [N][Hkv][B][d] of e4m3 codes as 2-D rows of d bytes; box = d
+// bytes (one 128-byte swizzle row for d = 128) x one block.
+int make_pool_map_u8(CUtensorMap *m, const void *pool, const pa_shape_t *sh) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)sh->head_dim,
+                                (cuuint64_t)sh->num_blocks * sh->num_kv_heads * sh->block_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)sh->head_dim};
+    const cuuint32_t box[2] = {(cuuint32_t)sh->head_dim, (cuuint32_t)sh->block_size};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(fp8 pool) failed");
+    return PA_OK;
+}
+
 // Packed rows [T][H][d] bf16; box = 64 columns x 1 head x box_rows rows.
 int make_rows_map(CUtensorMap *m, const void *base, int head_dim, int heads, long long rows,
                   int box_rows = 128) {
@@ -168,7 +185,8 @@ int do_append(const pa_shape_t *sh, const void *k_new, const void *v_new, const 
 int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const void *v_pool,
               const int32_t *block_table, int max_blocks, const int32_t *seq_lens, int num_seqs,
               int max_seq_len, void *out, void *ws, size_t ws_bytes, cudaStream_t st, DevState *d,
-              int check_first) {
+              int check_first, const float *k_scale = nullptr, const float *v_scale = nullptr) {
+    const bool fp8 = k_scale != nullptr;
     const int split = decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len, sh->block_size,
                                           d->num_sms, g_split_override.load());
     const int max_splits = decode_max_splits(max_seq_len, split);
@@ -177,11 +195,13 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
         return fail(PA_ERR_WORKSPACE, "workspace smaller than " + std::to_string(need) + " bytes");
     if (need > 0 && !aligned16(ws)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     CUtensorMap tk, tv;
-    int rc = make_pool_map(&tk, k_pool, sh);
+    int rc = fp8 ? make_pool_map_u8(&tk, k_pool, sh) : make_pool_map(&tk, k_pool, sh);
     if (rc) return rc;
-    rc = make_pool_map(&tv, v_pool, sh);
+    rc = fp8 ? make_pool_map_u8(&tv, v_pool, sh) : make_pool_map(&tv, v_pool, sh);
     if (rc) return rc;
     DecodeArgs a{};
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.block_table = block_table;
     a.seq_lens = seq_lens;
@@ -201,7 +221,7 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
     a.max_seq_len = max_seq_len;
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
-    cudaError_t e = launch_decode(tk, tv, a, sh->head_dim, sh->block_size, st);
+    cudaError_t e = launch_decode(tk, tv, a, sh->head_dim, sh->block_size, st, fp8);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return PA_OK;
 }
@@ -491,6 +511,78 @@ int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const 
     }
     rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                    out, workspace, ws_bytes, st, d, val);
+    if (rc) return rc;
+    return ok();
+}
+
+int pa_kv_append_fp8(const pa_shape_t *shape, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                     int num_tokens, const float *k_scale, const float *v_scale, void *k_pool, void *v_pool,
+                     void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (num_tokens == 0) return ok();
+    if (!k_new || !v_new || !slot_mapping || !k_scale || !v_scale || !k_pool || !v_pool)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return fail(PA_ERR_INVALID_ARG, "k/v and pools must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.slot_mapping = slot_mapping;
+        ca.num_tokens = num_tokens;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    cudaError_t e = launch_kv_append_fp8(static_cast<const __nv_bfloat16 *>(k_new),
+                                         static_cast<const __nv_bfloat16 *>(v_new), slot_mapping, num_tokens,
+                                         shape->num_kv_heads, shape->head_dim, shape->block_size, shape->num_blocks,
+                                         k_scale, v_scale, static_cast<uint8_t *>(k_pool),
+                                         static_cast<uint8_t *>(v_pool), d->err, val, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append_fp8 launch");
+    return ok();
+}
+
+int pa_decode_fp8(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
+                  const float *k_scale, const float *v_scale, const int32_t *block_table, int max_blocks_per_seq,
+                  const int32_t *seq_lens, int num_seqs, int max_seq_len, void *out, void *workspace,
+                  size_t ws_bytes, void *stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (shape->head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "fp8 decode supports head_dim 128");
+    if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_seqs == 0) return ok();
+    if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !block_table || !seq_lens || !out)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if ((max_seq_len + shape->block_size - 1) / shape->block_size > max_blocks_per_seq)
+        return fail(PA_ERR_INVALID_ARG, "max_seq_len does not fit in max_blocks_per_seq blocks");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PA_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.block_table = block_table;
+        ca.seq_lens = seq_lens;
+        ca.num_seqs = num_seqs;
+        ca.max_blocks = max_blocks_per_seq;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.max_seq_len = max_seq_len;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                   out, workspace, ws_bytes, st, d, val, k_scale, v_scale);
     if (rc) return rc;
     return ok();
 }

@@ -21,6 +21,7 @@ struct DecodeArgs {
     int split_tokens, max_splits, max_seq_len;
     int check_err_first;         // validation mode: skip work if *err != 0
     float scale_log2;            // softmax scale * log2(e)
+    const float *k_scale, *v_scale;  // fp8 pools: [Hkv] scales (value = code * scale); else null
 };
 
 // Tokens per split-K chunk chosen for a decode batch (multiple of block_size).
@@ -30,7 +31,7 @@ int decode_max_splits(int max_seq_len, int split_tokens);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits);
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, int block_size, cudaStream_t stream);
+                          int head_dim, int block_size, cudaStream_t stream, bool fp8 = false);
 
 // ------------------------------------------------------------- append ------
 cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
@@ -40,6 +41,13 @@ cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_
                              cudaStream_t stream);
 
 // Whole-block copies between pools (device or pinned host memory).
+// Append with quantisation to e4m3 codes (one scale per KV head).
+cudaError_t launch_kv_append_fp8(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
+                                 const int32_t *slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, const float *k_scale, const float *v_scale,
+                                 uint8_t *k_pool, uint8_t *v_pool, int *err, int check_err_first,
+                                 cudaStream_t stream);
+
 // Rotary embedding of a step's new tokens fused with their KV append.
 struct RopeArgs {
     const __nv_bfloat16 *q, *k_new, *v_new;

@@ -3,6 +3,7 @@
     python -m paged_kv_cache_continuous_gb300.profile_cases decode [num_seqs] [llama7b|long]
     python -m paged_kv_cache_continuous_gb300.profile_cases prefill 4096 | 1024,1024,1024,1024
     python -m paged_kv_cache_continuous_gb300.profile_cases append
+    python -m paged_kv_cache_continuous_gb300.profile_cases decode_fp8 [num_seqs]
 
 Each case builds its seeded workload on cuda:0, makes three warm-up calls and
 then one more, so `ncu -k regex:<kernel> -s 3 -c 1` captures a warm launch.
@@ -39,6 +40,23 @@ def decode(num_seqs: int = 128, which: str = "llama7b"):
     print(f"decode {which} seqs={st.num_seqs} split={split} max_splits={nsplit} kv_bytes={kv}")
 
 
+def decode_fp8(num_seqs: int = 128):
+    """The Llama-7B-shaped decode step over fp8 (e4m3) pools."""
+    shape, _, _, st = wl.llama7b_decode(pool_device=None, num_seqs=num_seqs)
+    N, H, B, d = shape.num_blocks, shape.num_kv_heads, shape.block_size, shape.head_dim
+    g = torch.Generator(device="cuda").manual_seed(1)
+    kp = torch.randint(0, 126, (N, H, B, d), dtype=torch.uint8, device="cuda", generator=g)
+    vp = torch.randint(0, 126, (N, H, B, d), dtype=torch.uint8, device="cuda", generator=g)
+    ks = torch.full((H,), 0.02, dtype=torch.float32, device="cuda")
+    q, bt, lens = _d(st.q), _d(st.block_table), _d(st.seq_lens)
+    ws = pa.workspace(shape, st.num_seqs, st.max_seq_len)
+    out = torch.empty_like(q)
+    for _ in range(4):
+        pa.decode_fp8(shape, q, kp, vp, ks, ks, bt, lens, st.max_seq_len, out=out, ws=ws)
+    pa.check_device_error()
+    print(f"decode_fp8 seqs={st.num_seqs}")
+
+
 def prefill(prompts):
     shape, kp, vp, st = wl.prefill_only(64, prompts, pool_device="cuda")
     pa.kv_append(shape, _d(st.k_new), _d(st.v_new), _d(st.slot_mapping), kp, vp)
@@ -69,6 +87,8 @@ def main(argv):
         prefill([int(x) for x in (argv[2] if len(argv) > 2 else "4096").split(",")])
     elif case == "append":
         append()
+    elif case == "decode_fp8":
+        decode_fp8(int(argv[2]) if len(argv) > 2 else 128)
     else:
         raise SystemExit(f"unknown case {case}")
 
