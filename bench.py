@@ -247,6 +247,7 @@ def run_ours(args, world, rank, local):
     copy = measure_copy(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
     rope = measure_rope(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
     fp8 = measure_fp8_decode(pa, wl, dev, hbm_peak, max(20, min(args.steps, 500))) if rank == 0 else None
+    serving = [measure_serving(dev, c) for c in (False, True)] if rank == 0 else None
 
     clocks = clk.summary()
     traffic = load_traffic("decode_splitk", nbytes, st.num_seqs)
@@ -276,6 +277,7 @@ def run_ours(args, world, rank, local):
         "block_copy": copy,
         "rope_append": rope,
         "fp8_decode": fp8,
+        "serving_loop": serving,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kp, vp, st, split, args.cpu_seconds)
@@ -536,6 +538,32 @@ def measure_fp8_decode(pa, wl, dev, hbm_peak, steps):
             "GBps": round(fp8_bytes / t / 1e9, 1), "frac_hbm": round(fp8_bytes / t / 1e9 / hbm_peak, 4),
             "algorithmic_bytes": int(fp8_bytes), "sequences_per_s": round(st.num_seqs / t, 1),
             "l2": "inputs larger than L2 (fp8 pools 1.2 GB)"}
+
+
+def measure_serving(dev, chunking: bool):
+    """Closed-loop continuous batching (host scheduler + one pa_mixed_step per
+    step, mock activations): 512 requests arrive at once, prompts U[16, 512],
+    U[64, 256] new tokens each, Hq 32 / Hkv 8 / d 128, B 16; run until all
+    are done.  Wall-clock over the whole run (host planning, H2D of the step's
+    index arrays and the GPU step), and the GPU time of the steps alone."""
+    from paged_kv_cache_continuous_gb300 import workload as wl
+    from paged_kv_cache_continuous_gb300.serving import ServingLoop
+    import time
+    shape = wl.Shape(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, num_blocks=26000)
+    loop = ServingLoop(shape, device=dev, seed=11, max_batch_prefill_tokens=4096, chunking=chunking,
+                       max_input_tokens=1024, max_total_tokens=2048, max_seqs=1024, max_tokens=8192)
+    rng = np.random.default_rng(12)
+    for i in range(512):
+        loop.submit(i, int(rng.integers(16, 513)), int(rng.integers(64, 257)))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    while loop.step() is not None:
+        pass
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    return {"requests": 512, "steps": loop.steps, "generated_tokens": loop.generated, "wall_s": round(wall, 4),
+            "tokens_per_s": round(loop.generated / wall, 1), "ms_per_step": round(wall / loop.steps * 1e3, 4),
+            "chunking": chunking}
 
 
 # ------------------------------------------------------------ CPU oracle --

@@ -33,6 +33,8 @@ EXPORTS = [
     "pa_set_decode_split",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
     "pa_alloc_num_free", "pa_alloc_num_blocks_of", "pa_alloc_block_table",
+    "pa_sched_create", "pa_sched_destroy", "pa_sched_submit", "pa_sched_cancel", "pa_sched_plan",
+    "pa_sched_commit", "pa_sched_stats",
     "pa_alloc_slot_mapping",
 ]
 
@@ -47,6 +49,13 @@ class PaShape(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+class SchedParams(ctypes.Structure):
+    _fields_ = [("max_batch_prefill_tokens", ctypes.c_int), ("max_batch_total_tokens", ctypes.c_int),
+                ("max_waiting_tokens", ctypes.c_int), ("waiting_served_ratio", ctypes.c_float),
+                ("max_batch_size", ctypes.c_int), ("chunking", ctypes.c_int),
+                ("max_input_tokens", ctypes.c_int), ("max_total_tokens", ctypes.c_int)]
 
 
 _lib = None
@@ -92,6 +101,13 @@ def load():
         "pa_alloc_num_blocks_of": ([P, ctypes.c_int64], I),
         "pa_alloc_block_table": ([P, P, I, I, ctypes.c_int32, P], I),
         "pa_alloc_slot_mapping": ([P, P, P, P, I, P], I),
+        "pa_sched_create": ([ctypes.POINTER(SchedParams), I, I], P),
+        "pa_sched_destroy": ([P], None),
+        "pa_sched_submit": ([P, ctypes.c_int64, I, I], I),
+        "pa_sched_cancel": ([P, ctypes.c_int64], I),
+        "pa_sched_plan": ([P, I, I, I, P, P, P, P, P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)], I),
+        "pa_sched_commit": ([P, P, I, ctypes.POINTER(I)], I),
+        "pa_sched_stats": ([P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -365,3 +381,66 @@ class BlockAllocator:
         if rc != OK:
             raise PagedAttnError(rc, "slot_mapping failed")
         return out
+
+
+class Scheduler:
+    """The host continuous-batching scheduler (include/pa_sched.h).  plan()
+    returns the arrays of one pa_mixed_step (numpy, host), or None when
+    nothing is to run; commit() advances the step and returns the finished
+    request ids."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_batch_prefill_tokens: int = 4096,
+                 max_batch_total_tokens: int = 0, max_waiting_tokens: int = 20, waiting_served_ratio: float = 1.2,
+                 max_batch_size: int = 0, chunking: bool = False, max_input_tokens: int = 1024,
+                 max_total_tokens: int = 2048, max_seqs: int = 4096, max_tokens: int = 65536, width: int = 1024):
+        lib = load()
+        self.params = SchedParams(max_batch_prefill_tokens, max_batch_total_tokens, max_waiting_tokens,
+                                  waiting_served_ratio, max_batch_size, int(chunking), max_input_tokens,
+                                  max_total_tokens)
+        self._h = lib.pa_sched_create(ctypes.byref(self.params), int(num_blocks), int(block_size))
+        if not self._h:
+            raise ValueError("pa_sched_create: bad arguments")
+        self.max_seqs, self.max_tokens, self.width = max_seqs, max_tokens, width
+        self._ids = np.zeros(max_seqs, dtype=np.int64)
+        self._qs = np.zeros(max_seqs + 1, dtype=np.int32)
+        self._lens = np.zeros(max_seqs, dtype=np.int32)
+        self._bt = np.zeros((max_seqs, width), dtype=np.int32)
+        self._slots = np.zeros(max_tokens, dtype=np.int32)
+        self._fin = np.zeros(max_seqs, dtype=np.int64)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            load().pa_sched_destroy(h)
+            self._h = None
+
+    def submit(self, request_id: int, input_tokens: int, max_new_tokens: int):
+        _check(load().pa_sched_submit(self._h, int(request_id), int(input_tokens), int(max_new_tokens)))
+
+    def cancel(self, request_id: int):
+        _check(load().pa_sched_cancel(self._h, int(request_id)))
+
+    def plan(self):
+        S, D, T = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+        p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+        _check(load().pa_sched_plan(self._h, self.max_seqs, self.max_tokens, self.width, p(self._ids), p(self._qs),
+                                    p(self._lens), p(self._bt), p(self._slots), ctypes.byref(S), ctypes.byref(D),
+                                    ctypes.byref(T)))
+        if S.value == 0:
+            return None
+        n = S.value
+        return {"seq_ids": self._ids[:n].copy(), "q_start_loc": self._qs[:n + 1].copy(),
+                "seq_lens": self._lens[:n].copy(), "block_table": self._bt[:n].copy(),
+                "slot_mapping": self._slots[:T.value].copy(), "num_decode": D.value, "num_tokens": T.value}
+
+    def commit(self):
+        nf = ctypes.c_int(0)
+        _check(load().pa_sched_commit(self._h, self._fin.ctypes.data_as(ctypes.c_void_p), self.max_seqs,
+                                      ctypes.byref(nf)))
+        return self._fin[:min(nf.value, self.max_seqs)].tolist()
+
+    def stats(self):
+        q, r, f, w = (ctypes.c_int(0) for _ in range(4))
+        _check(load().pa_sched_stats(self._h, ctypes.byref(q), ctypes.byref(r), ctypes.byref(f), ctypes.byref(w)))
+        return {"queued": q.value, "running": r.value, "free_blocks": f.value, "waiting_steps": w.value}
+

@@ -26,7 +26,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-r
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-I", str(ROOT / "include")]
 
 CU_SOURCES = ["pa_api.cu", "kv_append.cu", "decode.cu", "prefill_tc.cu", "prefill_tc2.cu", "block_copy.cu", "rope.cu"]
-CXX_SOURCES = ["block_alloc.cpp"]
+CXX_SOURCES = ["block_alloc.cpp", "scheduler.cpp"]
 
 
 def nvcc() -> str:
