@@ -517,8 +517,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (kk == 3) pass_turn();
                     }
                 };
+                // Every unit's Q is waited for, even by a thread with nothing to
+                // issue in it: its q_free commit below must not reach the
+                // buffer's barrier before the phase of unit ord - 2 is over.
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait_spin(&q_full[qb], (ord >> 1) & 1, a.err));
                 if (nk > 0) {
-                    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_spin(&q_full[qb], (ord >> 1) & 1, a.err));
                     wait_tile(0);
                     take_turn(0);
                     if (ok) {
@@ -649,6 +652,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int qb = ord & 1;
             ++ord;
             if (nk == 0) {  // nothing of this sub-tile in the unit: its Q buffer half is not staged
+                // Arrive for this unit only once the buffer's phase of unit
+                // ord - 3 (its previous user; ord already counts this unit) is
+                // over: warps with nothing to do run ahead, and an early
+                // arrival would count toward that phase and free the buffer
+                // while it is still read.
+                if (ord >= 3 && !wait_warp(&q_free[qb], (uint32_t)((((ord - 1) >> 1) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
                 if (lane == 0) mbar_arrive(&q_free[qb]);
                 continue;
             }
