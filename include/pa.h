@@ -296,6 +296,17 @@ const char *pa_last_error(void);
  */
 int pa_set_decode_split(int tokens);
 
+/*
+ * Prefill CTA-pair count override, for tests: with few pairs each pair walks
+ * many work units in turn, so the hand-offs between consecutive units (Q
+ * buffers, K/V ring stages, output staging) are exercised on every launch.
+ * pairs = 0 restores the automatic choice (one pair per two SMs, at most one
+ * per work unit); larger values are capped at that.  Returns PA_OK, or
+ * PA_ERR_INVALID_ARG for pairs < 0.  Applies to pa_prefill and the prefill
+ * part of pa_mixed_step.
+ */
+int pa_set_prefill_pairs(int pairs);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,6 +31,7 @@ EXPORTS = [
     "pa_decode_noalloc", "pa_prefill",
     "pa_mixed_step", "pa_copy_blocks", "pa_rope_append", "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_validation", "pa_check_device_error", "pa_last_error",
     "pa_set_decode_split",
+    "pa_set_prefill_pairs",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
     "pa_alloc_num_free", "pa_alloc_num_blocks_of", "pa_alloc_block_table",
     "pa_sched_create", "pa_sched_destroy", "pa_sched_submit", "pa_sched_cancel", "pa_sched_plan",
@@ -93,6 +94,7 @@ def load():
         "pa_check_device_error": ([P], I),
         "pa_last_error": ([], ctypes.c_char_p),
         "pa_set_decode_split": ([I], I),
+        "pa_set_prefill_pairs": ([I], I),
         "pa_alloc_create": ([I, I, P], P),
         "pa_alloc_destroy": ([P], None),
         "pa_alloc_ensure": ([P, ctypes.c_int64, I], I),
@@ -318,6 +320,10 @@ def set_validation(on: bool):
 
 def set_decode_split(tokens: int):
     _check(load().pa_set_decode_split(int(tokens)))
+
+
+def set_prefill_pairs(pairs: int):
+    _check(load().pa_set_prefill_pairs(int(pairs)))
 
 
 def check_device_error(stream=None):

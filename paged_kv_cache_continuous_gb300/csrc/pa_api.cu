@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -20,6 +21,7 @@ using namespace pa;
 thread_local std::string t_last_error;
 std::atomic<int> g_validation{0};
 std::atomic<int> g_split_override{0};
+std::atomic<int> g_pairs_override{0};  // prefill CTA pairs (0: automatic)
 
 // Device error word: kernels record PA_ERR_BAD_INDEX / PA_ERR_TIMEOUT here
 // instead of trapping; pa_check_device_error reads and clears it.
@@ -260,7 +262,10 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
     a.num_q_tiles = (max_q_len + 127) / 128;
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
-    a.num_sms = d->num_sms;
+    {
+        const int ov = g_pairs_override.load();
+        a.num_sms = ov > 0 ? std::min(2 * ov, d->num_sms) : d->num_sms;
+    }
     cudaError_t e;
     if (sh->head_dim == 128) {
         CUtensorMap to;
@@ -761,6 +766,12 @@ int pa_set_validation(int on) {
 int pa_set_decode_split(int tokens) {
     if (tokens < 0) return fail(PA_ERR_INVALID_ARG, "tokens < 0");
     g_split_override.store(tokens);
+    return ok();
+}
+
+int pa_set_prefill_pairs(int pairs) {
+    if (pairs < 0) return fail(PA_ERR_INVALID_ARG, "pairs < 0");
+    g_pairs_override.store(pairs);
     return ok();
 }
 

@@ -117,3 +117,6 @@ def test_workspace_size(lib):
     assert n.value == 2 * 32 * (-(-2049 // 64)) * 130 * 4
     assert lib.pa_set_decode_split(0) == 0
     assert lib.pa_set_decode_split(-1) == binding.ERR_INVALID_ARG
+    assert lib.pa_set_prefill_pairs(3) == 0
+    assert lib.pa_set_prefill_pairs(0) == 0
+    assert lib.pa_set_prefill_pairs(-1) == binding.ERR_INVALID_ARG

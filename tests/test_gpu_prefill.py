@@ -99,6 +99,44 @@ def test_prefill_paged_with_prefix(cuda_lib, Hq, Hkv, d, B):
     assert_close(out, ref, f"paged prefill Hq={Hq} Hkv={Hkv} d={d} B={B}")
 
 
+@pytest.mark.parametrize("pairs", [1, 3])
+@pytest.mark.parametrize("Hq,Hkv", [(24, 8), (32, 8), (16, 16), (16, 8)])
+def test_prefill_few_pairs(cuda_lib, pairs, Hq, Hkv):
+    """One or three CTA pairs: every pair walks dozens of work units in turn,
+    most with idle sub-tiles (short prompts), so each hand-off between
+    consecutive units -- a Q buffer reused two units later, the K/V ring,
+    output staging, the last V tile's tail -- is crossed many times in one
+    launch.  Idle warps that ran ahead once freed a Q buffer still in use."""
+    lens = [1, 7, 127, 128, 129, 300, 513, 40, 1000, 65]
+    shape, q, k, v, cu = _dense_case(29, lens, Hq, Hkv, 128)
+    pa.set_prefill_pairs(pairs)
+    try:
+        out = pa.prefill(shape, dev(q), dev(k), dev(v), dev(cu), max(lens))
+        pa.check_device_error()
+    finally:
+        pa.set_prefill_pairs(0)
+    ref = oracle.prefill(bits(q), bits(k), bits(v), cu)
+    assert_close(out, ref, f"dense prefill on {pairs} pair(s) Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_prefill_paged_few_pairs(cuda_lib, pairs):
+    case = [(0, 1), (5, 200), (130, 129), (1000, 64), (17, 300), (0, 256), (64, 3), (0, 700)]
+    shape, kp, vp, st, pre = _paged_case(24, case, 24, 8, 128, 16)
+    kd, vd = dev(kp), dev(vp)
+    pa.kv_append(shape, dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), kd, vd)
+    pa.set_prefill_pairs(pairs)
+    try:
+        out = pa.prefill(shape, dev(st.q), kd, vd, dev(st.q_start_loc), st.max_q_len,
+                         prefix_lens=dev(pre), block_table=dev(st.block_table))
+        pa.check_device_error()
+    finally:
+        pa.set_prefill_pairs(0)
+    kq, vq = oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, bits(kp), bits(vp))
+    ref = oracle.prefill(bits(st.q), kq, vq, st.q_start_loc, prefix_lens=pre, block_table=st.block_table)
+    assert_close(out, ref, f"paged prefill on {pairs} pair(s)")
+
+
 def test_decode_equals_last_prefill_row(cuda_lib):
     """(d) decode of token t equals row t of causal prefill over the sequence."""
     shape, kp, vp, pre, dec, full = wl.tiny()
