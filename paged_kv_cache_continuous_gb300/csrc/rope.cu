@@ -24,7 +24,8 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTok = 4;  // tokens per CTA pass: their cos / sin first, then all their rows at once
+constexpr int kTok = 4;    // tokens per CTA pass: their cos / sin first, then all their rows at once
+constexpr int kItems = 4;  // work items a thread holds in registers at once
 
 // Rotate eight pairs (i .. i+7 with i+d/2 .. i+d/2+7) of one head row: lo / hi
 // are 8 bf16 each (16 bytes); cs holds (cos, sin) of the eight pairs.
@@ -53,58 +54,79 @@ __global__ void __launch_bounds__(kThreads)
     const long long num_slots = (long long)a.num_blocks * a.block_size;
     for (int t0 = blockIdx.x * tpc; t0 < a.num_tokens; t0 += gridDim.x * tpc) {
         const int nt = min(tpc, a.num_tokens - t0);
-        __syncthreads();  // the previous pass's tables are no longer read
-        for (int e = threadIdx.x; e < nt * half; e += kThreads) {
-            const int tt = e / half, i = e % half;
-            const int p = __ldg(a.positions + t0 + tt);
-            double ang = (double)max(p, 0) * a.inv_freq[i];
-            ang -= rint(ang * 0.15915494309189535) * 6.283185307179586;  // into [-pi, pi]
-            float sn, cn;
-            sincosf((float)ang, &sn, &cn);
-            cs[tt][i] = make_float2(cn, sn);
-            if (i == 0) {
-                const int sl = __ldg(a.slot_mapping + t0 + tt);
-                const bool pos_ok = p >= 0, slot_ok = (long long)sl < num_slots;
-                if (!pos_ok || !slot_ok) set_error(a.err, PA_ERR_BAD_INDEX);
-                s_pos_ok[tt] = pos_ok;
-                s_slot[tt] = (pos_ok && slot_ok) ? sl : -1;  // never write outside the pool
+        // Work items of the pass: one (token, head, chunk pair) each -- the
+        // queries first, then the keys, then the values.
+        const int nq = nt * a.num_q_heads * cpr, nk = nt * a.num_kv_heads * cpr;
+        const int total = nq + 2 * nk;
+        for (int b0 = 0; b0 < total; b0 += kThreads * kItems) {
+            // Every load of the batch is issued before anything waits on one
+            // (and, in a pass's first batch, before the tables are built).
+            uint4 lo[kItems], hi[kItems];
+            int meta[kItems];  // kind (0 q, 1 k, 2 v) | token << 2 | chunk << 4 | head << 8
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                const int e = b0 + j * kThreads + (int)threadIdx.x;
+                meta[j] = -1;
+                if (e < total) {
+                    int kind, ee, heads;
+                    if (e < nq) {
+                        kind = 0, ee = e, heads = a.num_q_heads;
+                    } else {
+                        kind = e - nq < nk ? 1 : 2;
+                        ee = e - nq - (kind == 2 ? nk : 0);
+                        heads = a.num_kv_heads;
+                    }
+                    const int tt = ee / (heads * cpr), r = ee % (heads * cpr);
+                    const int h = r / cpr, ch = r % cpr;
+                    const __nv_bfloat16 *src = kind == 0 ? a.q : (kind == 1 ? a.k_new : a.v_new);
+                    const size_t o = ((size_t)(t0 + tt) * heads + h) * d + ch * 8;
+                    lo[j] = *reinterpret_cast<const uint4 *>(src + o);
+                    hi[j] = *reinterpret_cast<const uint4 *>(src + o + half);
+                    meta[j] = kind | (tt << 2) | (ch << 4) | (h << 8);
+                }
             }
-        }
-        __syncthreads();
-        // queries: nt tokens x Hq rows x cpr chunk pairs
-        const int nq = nt * a.num_q_heads * cpr;
-        for (int e = threadIdx.x; e < nq; e += kThreads) {
-            const int tt = e / (a.num_q_heads * cpr), r = e % (a.num_q_heads * cpr);
-            if (!s_pos_ok[tt]) continue;
-            const int h = r / cpr, i = (r % cpr) * 8;
-            const size_t o = ((size_t)(t0 + tt) * a.num_q_heads + h) * d + i;
-            uint4 lo = *reinterpret_cast<const uint4 *>(a.q + o), hi = *reinterpret_cast<const uint4 *>(a.q + o + half);
-            rotate8(lo, hi, &cs[tt][i]);
-            *reinterpret_cast<uint4 *>(a.q_out + o) = lo;
-            *reinterpret_cast<uint4 *>(a.q_out + o + half) = hi;
-        }
-        // keys, rotated into the slot, and values, copied: nt tokens x Hkv rows
-        const int nk = nt * a.num_kv_heads * cpr;
-        for (int e = threadIdx.x; e < 2 * nk; e += kThreads) {
-            const bool is_v = e >= nk;
-            const int ee = is_v ? e - nk : e;
-            const int tt = ee / (a.num_kv_heads * cpr), r = ee % (a.num_kv_heads * cpr);
-            const int sl = s_slot[tt];
-            if (sl < 0) continue;
-            const int h = r / cpr, i = (r % cpr) * 8;
-            const size_t src = ((size_t)(t0 + tt) * a.num_kv_heads + h) * d + i;
-            const long long blk = sl / a.block_size, off = sl % a.block_size;
-            const size_t dst = ((size_t)(blk * a.num_kv_heads + h) * a.block_size + off) * d + i;
-            if (is_v) {
-                *reinterpret_cast<uint4 *>(a.v_pool + dst) = *reinterpret_cast<const uint4 *>(a.v_new + src);
-                *reinterpret_cast<uint4 *>(a.v_pool + dst + half) =
-                    *reinterpret_cast<const uint4 *>(a.v_new + src + half);
-            } else {
-                uint4 lo = *reinterpret_cast<const uint4 *>(a.k_new + src);
-                uint4 hi = *reinterpret_cast<const uint4 *>(a.k_new + src + half);
-                rotate8(lo, hi, &cs[tt][i]);
-                *reinterpret_cast<uint4 *>(a.k_pool + dst) = lo;
-                *reinterpret_cast<uint4 *>(a.k_pool + dst + half) = hi;
+            if (b0 == 0) {
+                __syncthreads();  // the previous pass's tables are no longer read
+                for (int e = threadIdx.x; e < nt * half; e += kThreads) {
+                    const int tt = e / half, i = e % half;
+                    const int p = __ldg(a.positions + t0 + tt);
+                    double ang = (double)max(p, 0) * a.inv_freq[i];
+                    ang -= rint(ang * 0.15915494309189535) * 6.283185307179586;  // into [-pi, pi]
+                    float sn, cn;
+                    sincosf((float)ang, &sn, &cn);
+                    cs[tt][i] = make_float2(cn, sn);
+                    if (i == 0) {
+                        const int sl = __ldg(a.slot_mapping + t0 + tt);
+                        const bool pos_ok = p >= 0, slot_ok = (long long)sl < num_slots;
+                        if (!pos_ok || !slot_ok) set_error(a.err, PA_ERR_BAD_INDEX);
+                        s_pos_ok[tt] = pos_ok;
+                        s_slot[tt] = (pos_ok && slot_ok) ? sl : -1;  // never write outside the pool
+                    }
+                }
+                __syncthreads();
+            }
+            // Rotate the queries (into q_out) and keys (into their pool slot);
+            // copy the values.
+#pragma unroll
+            for (int j = 0; j < kItems; ++j) {
+                if (meta[j] < 0) continue;
+                const int kind = meta[j] & 3, tt = (meta[j] >> 2) & 3, ch = (meta[j] >> 4) & 15, h = meta[j] >> 8;
+                const int i = ch * 8;
+                __nv_bfloat16 *dst;
+                if (kind == 0) {
+                    if (!s_pos_ok[tt]) continue;
+                    rotate8(lo[j], hi[j], &cs[tt][i]);
+                    dst = a.q_out + ((size_t)(t0 + tt) * a.num_q_heads + h) * d + i;
+                } else {
+                    const int sl = s_slot[tt];
+                    if (sl < 0) continue;
+                    if (kind == 1) rotate8(lo[j], hi[j], &cs[tt][i]);
+                    const long long blk = sl / a.block_size, off = sl % a.block_size;
+                    dst = (kind == 1 ? a.k_pool : a.v_pool) +
+                          ((size_t)(blk * a.num_kv_heads + h) * a.block_size + off) * d + i;
+                }
+                *reinterpret_cast<uint4 *>(dst) = lo[j];
+                *reinterpret_cast<uint4 *>(dst + half) = hi[j];
             }
         }
     }

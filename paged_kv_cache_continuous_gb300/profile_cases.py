@@ -4,6 +4,7 @@
     python -m paged_kv_cache_continuous_gb300.profile_cases prefill 4096 | 1024,1024,1024,1024
     python -m paged_kv_cache_continuous_gb300.profile_cases append
     python -m paged_kv_cache_continuous_gb300.profile_cases decode_fp8 [num_seqs]
+    python -m paged_kv_cache_continuous_gb300.profile_cases rope [num_tokens]
 
 Each case builds its seeded workload on cuda:0, makes three warm-up calls and
 then one more, so `ncu -k regex:<kernel> -s 3 -c 1` captures a warm launch.
@@ -77,6 +78,24 @@ def append():
     print(f"append tokens={st.num_tokens}")
 
 
+def rope(T: int = 4096, Hq: int = 32, Hkv: int = 8):
+    """Rotary embedding fused with the append, the bench's prompt step shape."""
+    g = torch.Generator().manual_seed(23)
+    nb = T // 16 + 16
+    shape = wl.Shape(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, block_size=16, num_blocks=nb)
+    q = wl.bf16_randn((T, Hq, 128), g).cuda()
+    k, v = wl.bf16_randn((T, Hkv, 128), g).cuda(), wl.bf16_randn((T, Hkv, 128), g).cuda()
+    kp = torch.zeros((nb, Hkv, 16, 128), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda")
+    slots = torch.randperm(nb * 16, generator=g)[:T].to(torch.int32).cuda()
+    q_out = torch.empty_like(q)
+    for _ in range(4):
+        pa.rope_append(shape, q, k, v, pos, slots, kp, vp, q_out=q_out)
+    pa.check_device_error()
+    print(f"rope tokens={T} Hq={Hq} Hkv={Hkv}")
+
+
 def main(argv):
     pa.load()
     torch.cuda.set_device(0)
@@ -89,6 +108,8 @@ def main(argv):
         append()
     elif case == "decode_fp8":
         decode_fp8(int(argv[2]) if len(argv) > 2 else 128)
+    elif case == "rope":
+        rope(int(argv[2]) if len(argv) > 2 else 4096)
     else:
         raise SystemExit(f"unknown case {case}")
 
