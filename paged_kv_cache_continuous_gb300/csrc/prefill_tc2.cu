@@ -23,8 +23,9 @@
 //     along N between the pair), both 64-column halves of d.
 //   V tile (128 keys): CTA c loads all keys, d columns 64c .. 64c+63.
 //   S_k = Q_k K^T (M=256, N=128, K=128) -> each CTA's TMEM S_k (128 columns).
-//   Softmax (thread = row = TMEM lane) writes P_k (bf16 pairs) over the first
-//     64 columns of S_k, then arrives on the leader.
+//   Softmax (two threads per row = TMEM lane, one per 64-key half) writes
+//     P_k (bf16 pairs) over S_k columns 0-31 (keys 0-63) and 64-95 (keys
+//     64-127), then arrives on the leader.
 //   O_k += P_k V (A from TMEM, M=256, N=128: the two d halves, K=128 keys).
 //   Per KV tile the leader issues PV_0(t), S_0(t+1), PV_1(t), S_1(t+1): while
 //   the tensor core works for one sub-tile the other's softmax runs.  S_k(t+1)
@@ -38,9 +39,13 @@
 // Warps: 0 and 1 issue (leader CTA only) the MMAs of sub-tiles 0 and 1 -- a
 // thread stalls for hundreds of cycles on each mbarrier test, and the other
 // thread's queued MMAs keep the tensor core busy meanwhile; warp 0 also
-// allocates TMEM (both CTAs); 2 TMA producer; 3-6 and 7-10 softmax for
-// sub-tiles 0 and 1 (warp w: rows 32 (w % 4) .. +31, TMEM lane quadrant
-// w % 4, all 128 columns).
+// allocates TMEM (both CTAs); 2 TMA producer; 3-10 softmax, for both sub-tiles
+// in turn (warp w: rows 32 (w % 4) .. +31, TMEM lane quadrant w % 4; warps
+// 3-6 keys 0-63 of each tile, 7-10 keys 64-127).  The two sub-tiles'
+// softmaxes alternate in time anyway (each waits on its own MMAs), so all
+// eight warps take each one: two warps per row on every SM sub-partition
+// roughly halve the softmax's latency, which sets the length of each
+// sub-tile's S -> softmax -> PV chain.
 // Loads signal the leader's barriers (cp.async.bulk.tensor .cta_group::2);
 // the leader's commits signal both CTAs (multicast).  The last V tile of a
 // unit is loaded against a local barrier in each CTA so its rows past the last
@@ -80,17 +85,18 @@ constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 * 4 + 1 + 2 + 2;
 // the units are dealt from a list in shared memory that holds non-empty units
 // only; otherwise every (level, head group, sequence) slot is dealt and empty
 // ones are skipped.
-constexpr int kSeqMax = 512;                             // sequences in the shared-memory schedule
-constexpr int kSeqInfoMax = 64;                          // ... with (row0, n, p0) cached there too
+constexpr int kSeqMax = 256;                             // sequences in the shared-memory schedule
+constexpr int kSeqInfoMax = 32;                          // ... with (row0, n, p0) cached there too
 constexpr int kMaxLevels = 64;                           // row-tile levels (units per head and sequence)
 constexpr int kSeqKeyOff = kBarOff + kNumBars * 8 + 16;  // uint8 [kSeqMax]: a sequence's levels
 constexpr int kSeqOrderOff = kSeqKeyOff + kSeqMax;       // uint16 [kSeqMax]: sequences, most levels first
 constexpr int kSeqInfoOff = kSeqOrderOff + kSeqMax * 2;  // int [kSeqInfoMax][3]: row0, n, p0
 constexpr int kLevelOff = kSeqInfoOff + kSeqInfoMax * 12;   // int [kMaxLevels + 1]: units above a level
 constexpr int kCountOff = kLevelOff + (kMaxLevels + 1) * 4; // int [kMaxLevels + 1]: scratch counts
-constexpr int kSmemBytes = kCountOff + (kMaxLevels + 1) * 4;
+constexpr int kXchgOff = kCountOff + (kMaxLevels + 1) * 4;  // float [kBM]: a row's max / sum between its halves
+constexpr int kSmemBytes = kXchgOff + kBM * 4;
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kSeqInfoOff % 4 == 0, "alignment");
+static_assert(kSeqInfoOff % 4 == 0 && kXchgOff % 4 == 0, "alignment");
 
 struct RowTile {
     int h, q0, rows, kv_end;
@@ -215,9 +221,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t *tile_full = q_free + 2;           // [kStages] leader: K and V of a tile landed in both CTAs
     uint64_t *tile_free = tile_full + kStages;  // [kStages] both sub-tiles' MMAs on the tile have completed
     uint64_t *s_full = tile_free + kStages;     // [2] S_k(t) is in TMEM (commit, both CTAs)
-    uint64_t *p_full = s_full + 2;              // [2] leader: P_k(t) stored by the 8 softmax warps of the pair
+    uint64_t *p_full = s_full + 2;              // [2] leader: P_k(t) stored by the 16 softmax warps of the pair
     uint64_t *o_done = p_full + 2;              // [2] a unit's last PV_k has completed (commit, both CTAs)
-    uint64_t *o_free = o_done + 2;              // [2] leader: the 8 softmax warps have read O_k out
+    uint64_t *o_free = o_done + 2;              // [2] leader: the 16 softmax warps have read O_k out
     uint64_t *v_last = o_free + 2;              // local: this CTA's half of a unit's last V tile landed
     uint64_t *v_tail = v_last + 1;              // [2] leader (unit parity): both halves zeroed past the last key
     uint64_t *mma_fin = v_tail + 2;             // [2] leader: every MMA issued by thread k has completed
@@ -295,9 +301,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&q_full[b], 1);
             mbar_init(&q_free[b], 2 + 8);  // one commit per issuing thread, one arrival per softmax warp
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 2 * 4);  // one arrival per softmax warp of each CTA
+            mbar_init(&p_full[b], 2 * 8);  // one arrival per softmax warp of each CTA
             mbar_init(&o_done[b], 1);
-            mbar_init(&o_free[b], 2 * 4);
+            mbar_init(&o_free[b], 2 * 8);
             mbar_init(&v_tail[b], 2);
             mbar_init(&mma_fin[b], 1);
         }
@@ -543,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint64_t bv = dv0 + (uint64_t)((((gb + t) % kStages) * kStageBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
-                        umma_bf16_pair_tmem_a_w(tO, tS + kk * 8, bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
+                        umma_bf16_pair_tmem_a_w(tO, tS + (kk >> 2) * 64 + (kk & 3) * 8, bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
                                               (t > 0 || kk > 0) ? 1u : 0u);
                         if (kk == 3 && !more) pass_turn();
                     }
@@ -573,34 +579,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ----------------------------------------------------------- softmax --
-        // Warps 3+4k .. 6+4k do sub-tile k; warp w owns rows 32q .. 32q+31 (TMEM
-        // lane quadrant q), one row per thread, all 128 columns.
-        const int k = (warp - kSoftmaxWarp0) >> 2, q = warp & 3;
+        // All eight warps serve both sub-tiles, one tile at a time: warp w owns
+        // rows 32q .. 32q+31 (q = w % 4, its TMEM lane quadrant and its SM
+        // sub-partition) and key half hf of every tile -- S columns 64 hf ..
+        // 64 hf + 63, one thread per row -- so each sub-partition runs two
+        // warps on each tile's exponentials.  A thread's weights go to the
+        // first 32 of its columns (it only overwrites scores it has read).  The
+        // two warps of a quadrant share a row's running maximum and sum
+        // through a named barrier of 64 threads and one word per row in shared
+        // memory.
+        const int hf = (warp - kSoftmaxWarp0) >> 2, q = warp & 3;
         const int r = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const uint32_t tS = tmem + lane_base + k * kBN;
-        const uint32_t tO = tmem + lane_base + 2 * kBN + k * kD;
-        const uint32_t pf = map_to_cta(smem_u32(&p_full[k]), 0);
-        const uint32_t of = map_to_cta(smem_u32(&o_free[k]), 0);
+        const uint32_t bar_id = 1 + q;
+        float *xchg = reinterpret_cast<float *>(smem + kXchgOff) + r;
         const float sl = a.scale_log2;
         bool ok = true;
-        int sc = 0, uo = 0, lvl = 0, ord = 0;  // S_k phases seen, units of sub-tile k done, schedule cursor, units
+        int sc[2] = {0, 0}, uo[2] = {0, 0};  // S_k phases seen, units of sub-tile k done
+        int lvl = 0, ord = 0;                // schedule cursor, units
         auto wait_warp = [&](uint64_t *bb, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait(bb, par, a.err));
         };
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory"); };
+        // true in both warps of the quadrant if p holds for any of their threads
+        auto pair_any = [&](bool p) {
+            uint32_t res;
+            asm volatile(
+                "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+                "bar.red.or.pred po, %2, 64, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+                : "=r"(res)
+                : "r"((uint32_t)p), "r"(bar_id)
+                : "memory");
+            return res != 0u;
+        };
+        // The row's maximum (or sum) over both halves, the same bits in both
+        // threads: half 1 posts its value, half 0 combines and posts the
+        // result, half 1 reads it.  (A word is written again only after its
+        // reader has passed the next barrier.)
+        auto pair_combine = [&](float x, bool is_max) {
+            if (hf == 1) *xchg = x;
+            pair_sync();
+            if (hf == 0) {
+                const float y = *xchg;
+                x = is_max ? fmaxf(x, y) : x + y;
+                *xchg = x;
+            }
+            pair_sync();
+            if (hf == 1) x = *xchg;
+            return x;
+        };
         // One arrival per warp on the leader's barrier, after the warp's
         // tcgen05 work is ordered before it.
-        auto arrive_leader = [&](uint64_t *bb, uint32_t remote) {
+        auto arrive_leader = [&](uint64_t *bb) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 if (c == 0) mbar_arrive(bb);
-                else mbar_arrive_cluster(remote);
+                else mbar_arrive_cluster(map_to_cta(smem_u32(bb), 0));
             }
         };
-        // A row's scores are handled in two halves of 64 keys (64 registers
-        // live instead of 128, which leaves the compiler room to overlap the
-        // exponentials of many columns).
         auto row_max64 = [&](const float *x) {
             float m4[4];
 #pragma unroll
@@ -615,9 +652,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 64; ++j) x[j] = j < lim ? x[j] : -INFINITY;
         };
-        // P = exp2(scale * S - mu) for 64 keys as 32 bf16 pairs at TMEM column
-        // `pcol` of S_k (column j: keys 2j, 2j+1 of the half); returns the row
-        // sum of the same rounded weights.  The TMEM stores are left in flight.
+        // P = exp2(scale * S - mu) for this half's 64 keys as 32 bf16 pairs at
+        // TMEM columns pcol .. pcol + 31 (column j: keys 2j, 2j+1 of the half);
+        // returns the row sum of the same rounded weights.  The TMEM stores
+        // are left in flight.
         auto exps64_to_tmem = [&](const float *x, float mu, uint32_t pcol) {
             float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -633,9 +671,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             return (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
         };
-        auto rescale_o = [&](float alpha) {
+        auto rescale_o = [&](uint32_t tO, float alpha) {  // this half's 64 columns of O_k
 #pragma unroll 1
-            for (int cc = 0; cc < kD / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 float o[32];
                 tmem_ld32(tO + cc * 32, o);
 #pragma unroll
@@ -648,141 +686,104 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (v >= num_units) continue;
             Unit u;
             if (!unit_at<PAGED, BS, MODE>(a, smem, compact, npx, ny, v, lvl, u)) continue;
-            const int nk = k ? u.nkt1 : u.nkt0;
             const int qb = ord & 1;
             ++ord;
-            if (nk == 0) {  // nothing of this sub-tile in the unit: its Q buffer half is not staged
-                // Arrive for this unit only once the buffer's phase of unit
-                // ord - 3 (its previous user; ord already counts this unit) is
-                // over: warps with nothing to do run ahead, and an early
-                // arrival would count toward that phase and free the buffer
-                // while it is still read.
-                if (ord >= 3 && !wait_warp(&q_free[qb], (uint32_t)((((ord - 1) >> 1) - 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) mbar_arrive(&q_free[qb]);
-                continue;
-            }
-            const RowTile my = my_tile<MODE>(u, c, k);
-            const int lim_abs = min(u.p0 + my.q0 + r + 1, my.kv_end);  // keys visible to row r
-            float m_run = 0.f, l_run = 0.f;
-            for (int t = 0; t < nk; ++t) {
-                // S_k(t) completing also means PV_k(t-1) has: O_k is stable and
-                // P_k(t-1) is no longer needed.
-                if (!wait_warp(&s_full[k], sc & 1)) {
-                    ok = false;
-                    break;
-                }
-                ++sc;
-                tc_fence_after();
-                const int lim = lim_abs - t * kBN;  // visible columns of this row
-                // Warp-uniform branch: only tiles crossing some row's last key pay
-                // for the mask.
-                const bool masked = __any_sync(0xffffffffu, lim < kBN);
-                if (t == 0) {
-                    // key 0 is visible to every row, so the first tile's maximum is finite
+            const int nk[2] = {u.nkt0, u.nkt1};
+            const RowTile my[2] = {my_tile<MODE>(u, c, 0), my_tile<MODE>(u, c, 1)};
+            int lim_abs[2];  // keys of this half visible to row r, per sub-tile
+            float m_run[2] = {0.f, 0.f}, l_run[2] = {0.f, 0.f};  // l_run: this half's share of the row sum
+#pragma unroll
+            for (int k = 0; k < 2; ++k) lim_abs[k] = min(u.p0 + my[k].q0 + r + 1, my[k].kv_end) - 64 * hf;
+            for (int t = 0; t < u.T && ok; ++t) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    if (t >= nk[k]) continue;
+                    const uint32_t tS = tmem + lane_base + k * kBN + 64 * hf;
+                    const uint32_t tO = tmem + lane_base + 2 * kBN + k * kD + 64 * hf;
+                    // S_k(t) completing also means PV_k(t-1) has: O_k is stable
+                    // and P_k(t-1) is no longer needed.  Both warps of the
+                    // quadrant take every barrier below whatever their waits
+                    // returned; a failed wait is acted on together.
+                    const bool got = wait_warp(&s_full[k], sc[k] & 1);
+                    ++sc[k];
+                    tc_fence_after();
+                    const int lim = lim_abs[k] - t * kBN;  // visible columns of this half
+                    // (Read even after a failed wait -- the values are then
+                    // unused.)  Warp-uniform branch: only tiles crossing some
+                    // row's last key pay for the mask.
                     float v[64];
                     tmem_ld64(tS, v);
-                    if (masked) mask64(v, lim);
-                    float mx = row_max64(v);
-                    tmem_ld64(tS + 64, v);
-                    if (masked) mask64(v, lim - 64);
-                    m_run = fmaxf(mx, row_max64(v)) * sl;
-                }
-                // Exponentials against the running maximum, half by half (P of
-                // keys 0-63 over S columns 0-31, whose scores are read; keys 64-127
-                // over columns 32-63, read with the first half).  A half's row sum
-                // shows when the maximum has grown too far (weights above 2^63 or
-                // not finite; never for t == 0): then move the maximum, rescale O_k
-                // (stable: PV_k(t-1) has completed) and an already written first
-                // half, and redo the half.
-                float l_tile = 0.f;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[64];
-                    tmem_ld64(tS + 64 * h, v);
-                    if (masked) mask64(v, lim - 64 * h);
-                    float lh = exps64_to_tmem(v, m_run, tS + 32 * h);
-                    if (t > 0 && __any_sync(0xffffffffu, !(lh <= 0x1p63f))) {
-                        float mx = row_max64(v);
-                        if (h == 0) {  // the second half's scores are still in S columns 64-127
-                            float w[64];
-                            tmem_ld64(tS + 64, w);
-                            if (masked) mask64(w, lim - 64);
-                            mx = fmaxf(mx, row_max64(w));
+                    if (__any_sync(0xffffffffu, lim < 64)) mask64(v, lim);
+                    // Key 0 is visible to every row, so the first tile's maximum
+                    // is finite; later tiles keep the running maximum unless a
+                    // weight would pass 2^63 (or is not finite): then the maximum
+                    // moves, O_k (stable) and the sums are rescaled and both
+                    // halves are redone.
+                    if (t == 0) m_run[k] = pair_combine(got ? row_max64(v) : -INFINITY, true) * sl;
+                    float lh = got ? exps64_to_tmem(v, m_run[k], tS) : 0.f;
+                    if (pair_any(!got || (t > 0 && !(lh <= 0x1p63f)))) {
+                        if (pair_any(!got)) {
+                            ok = false;
+                            break;
                         }
-                        const float m_new = fmaxf(m_run, mx * sl);
-                        const float alpha = fast_exp2(m_run - m_new);
-                        m_run = m_new;
-                        rescale_o(alpha);
-                        l_run *= alpha;
+                        const float m_new = fmaxf(m_run[k], pair_combine(row_max64(v), true) * sl);
+                        const float alpha = fast_exp2(m_run[k] - m_new);
+                        m_run[k] = m_new;
                         tmem_wait_st();
-                        if (h == 1) {  // the first half's weights, already in TMEM: scale and re-round
-                            uint32_t pk[32];
-                            tmem_ld32(tS, reinterpret_cast<float *>(pk));
-                            float2 ls2 = make_float2(0.f, 0.f);
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float2 w2 = bf16x2_unpack(pk[j]);
-                                pk[j] = pack_bf16x2(w2.x * alpha, w2.y * alpha);
-                                ls2 = add_f32x2(ls2, bf16x2_unpack(pk[j]));
-                            }
-                            tmem_st16_async(tS, pk);
-                            tmem_st16_async(tS + 16, pk + 16);
-                            l_tile = ls2.x + ls2.y;
-                        }
-                        lh = exps64_to_tmem(v, m_run, tS + 32 * h);
+                        lh = exps64_to_tmem(v, m_run[k], tS);
+                        rescale_o(tO, alpha);
+                        l_run[k] *= alpha;
                     }
-                    l_tile += lh;
+                    l_run[k] = (t == 0) ? lh : l_run[k] + lh;
+                    tmem_wait_st();
+                    arrive_leader(&p_full[k]);
                 }
-                l_run = (t == 0) ? l_tile : l_run + l_tile;
-                tmem_wait_st();
-                arrive_leader(&p_full[k], pf);
             }
             if (!ok) break;
             // ------------------------------------------------------ epilogue --
-            // Read O_k out, release it for the next unit, then normalise and store.
-            if (!wait_warp(&o_done[k], uo & 1)) {
-                ok = false;
-                break;
-            }
-            ++uo;
-            tc_fence_after();
-            float o[kD];
-            tmem_ld128(tO, o);
-            arrive_leader(&o_free[k], of);
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            if (32 * q + 32 <= my.rows) {
-                // All 32 rows of the warp are the sequence's: stage them in this
-                // sub-tile's Q buffer (every MMA reading it has completed) as two
-                // 64-column boxes of 32 swizzled 128-byte rows, and let TMA store
-                // them -- coalesced, and off the warp's instruction stream.
-                uint8_t *stg = smem + kQOff + (2 * qb + k) * kQBytes + q * 8192;
+            // Per sub-tile: read this half of O_k out, release it for the next
+            // unit, then normalise by the row sum of both halves and store.
 #pragma unroll
-                for (int j = 0; j < kD / 8; ++j) {
-                    const uint4 pk = make_uint4(pack_bf16x2(o[8 * j] * inv, o[8 * j + 1] * inv),
-                                                pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv),
-                                                pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv),
-                                                pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
-                    *reinterpret_cast<uint4 *>(stg + (j >> 3) * 4096 + lane * 128 + (((j & 7) ^ (lane & 7)) << 4)) =
-                        pk;
+            for (int k = 0; k < 2; ++k) {
+                if (nk[k] == 0) continue;
+                const uint32_t tO = tmem + lane_base + 2 * kBN + k * kD + 64 * hf;
+                const bool od = wait_warp(&o_done[k], uo[k] & 1);
+                ++uo[k];
+                tc_fence_after();
+                float o[64];
+                tmem_ld64(tO, o);
+                if (od) arrive_leader(&o_free[k]);
+                const float l_row = pair_combine(l_run[k], false);
+                if (pair_any(!od)) {
+                    ok = false;
+                    break;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int row = u.row0 + my.q0 + 32 * q;
-                    tma_store_3d(&tm_o, stg, 0, my.h, row);
-                    tma_store_3d(&tm_o, stg + 4096, 64, my.h, row);
-                    bulk_commit_group();
-                    bulk_wait_read_all();
-                    mbar_arrive(&q_free[qb]);
-                }
-            } else {
-                if (r < my.rows) {
-                    __nv_bfloat16 *orow = a.out + ((size_t)(u.row0 + my.q0 + r) * a.num_q_heads + my.h) * kD;
+                const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                if (32 * q + 32 <= my[k].rows) {
+                    // All 32 rows of the warp are the sequence's: stage them in
+                    // this sub-tile's Q buffer (every MMA reading it has
+                    // completed) as one 64-column box of 32 swizzled 128-byte
+                    // rows, and let TMA store it.
+                    uint8_t *stg = smem + kQOff + (2 * qb + k) * kQBytes + q * 8192 + hf * 4096;
 #pragma unroll
-                    for (int i = 0; i < kD; i += 8) {
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 pk = make_uint4(pack_bf16x2(o[8 * j] * inv, o[8 * j + 1] * inv),
+                                                    pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv),
+                                                    pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv),
+                                                    pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
+                        *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = pk;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tm_o, stg, 64 * hf, my[k].h, u.row0 + my[k].q0 + 32 * q);
+                        bulk_commit_group();
+                    }
+                } else if (r < my[k].rows) {
+                    __nv_bfloat16 *orow =
+                        a.out + ((size_t)(u.row0 + my[k].q0 + r) * a.num_q_heads + my[k].h) * kD + 64 * hf;
+#pragma unroll
+                    for (int i = 0; i < 64; i += 8) {
                         const uint4 pk = make_uint4(pack_bf16x2(o[i] * inv, o[i + 1] * inv),
                                                     pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
                                                     pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
@@ -790,7 +791,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(orow + i) = pk;
                     }
                 }
-                if (lane == 0) mbar_arrive(&q_free[qb]);
+            }
+            if (!ok) break;
+            // The unit's Q buffer is free once the stores have read the staging.
+            if (lane == 0) {
+                bulk_wait_read_all();
+                mbar_arrive(&q_free[qb]);
             }
         }
         if (lane == 0) bulk_wait_all();  // the output stores are done before the CTA exits
