@@ -45,7 +45,10 @@ __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float2 *cs) 
 
 __global__ void __launch_bounds__(kThreads)
     rope_append_kernel(const RopeArgs a, int tpc) {  // tpc <= kTok tokens per pass
-    __shared__ float2 cs[kTok][64];  // (cos, sin) per token of the pass and pair
+    // (cos, sin) per token of the pass and pair i, at i + i / 8: a thread reads
+    // the eight pairs of its 16-byte chunk, and the padding puts a warp's eight
+    // chunks on distinct banks.
+    __shared__ float2 cs[kTok][72];
     __shared__ int s_slot[kTok];     // the token's slot, or -1 if it is not appended (or skipped)
     __shared__ int s_pos_ok[kTok];
     if (a.check_err_first && *(volatile int *)a.err != 0) return;
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(kThreads)
                     ang -= rint(ang * 0.15915494309189535) * 6.283185307179586;  // into [-pi, pi]
                     float sn, cn;
                     sincosf((float)ang, &sn, &cn);
-                    cs[tt][i] = make_float2(cn, sn);
+                    cs[tt][i + (i >> 3)] = make_float2(cn, sn);
                     if (i == 0) {
                         const int sl = __ldg(a.slot_mapping + t0 + tt);
                         const bool pos_ok = p >= 0, slot_ok = (long long)sl < num_slots;
@@ -115,12 +118,12 @@ __global__ void __launch_bounds__(kThreads)
                 __nv_bfloat16 *dst;
                 if (kind == 0) {
                     if (!s_pos_ok[tt]) continue;
-                    rotate8(lo[j], hi[j], &cs[tt][i]);
+                    rotate8(lo[j], hi[j], &cs[tt][i + ch]);
                     dst = a.q_out + ((size_t)(t0 + tt) * a.num_q_heads + h) * d + i;
                 } else {
                     const int sl = s_slot[tt];
                     if (sl < 0) continue;
-                    if (kind == 1) rotate8(lo[j], hi[j], &cs[tt][i]);
+                    if (kind == 1) rotate8(lo[j], hi[j], &cs[tt][i + ch]);
                     const long long blk = sl / a.block_size, off = sl % a.block_size;
                     dst = (kind == 1 ? a.k_pool : a.v_pool) +
                           ((size_t)(blk * a.num_kv_heads + h) * a.block_size + off) * d + i;

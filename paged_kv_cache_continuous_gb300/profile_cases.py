@@ -5,6 +5,7 @@
     python -m paged_kv_cache_continuous_gb300.profile_cases append
     python -m paged_kv_cache_continuous_gb300.profile_cases decode_fp8 [num_seqs]
     python -m paged_kv_cache_continuous_gb300.profile_cases rope [num_tokens]
+    python -m paged_kv_cache_continuous_gb300.profile_cases copy [num_pairs]
 
 Each case builds its seeded workload on cuda:0, makes three warm-up calls and
 then one more, so `ncu -k regex:<kernel> -s 3 -c 1` captures a warm launch.
@@ -96,6 +97,21 @@ def rope(T: int = 4096, Hq: int = 32, Hkv: int = 8):
     print(f"rope tokens={T} Hq={Hq} Hkv={Hkv}")
 
 
+def copy(num_pairs: int = 1024):
+    """A block fork inside one pool pair (the bench's block shape: 32 KV heads x
+    16 tokens x 128 dims, 128 KB per block and pool)."""
+    N = 2 * num_pairs
+    shape = wl.Shape(num_q_heads=32, num_kv_heads=32, head_dim=128, block_size=16, num_blocks=N)
+    kp = torch.empty((N, 32, 16, 128), dtype=torch.bfloat16, device="cuda").normal_()
+    vp = torch.empty_like(kp).normal_()
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(17)).to(torch.int32)
+    src, dst = perm[:num_pairs].cuda(), perm[num_pairs:].cuda()
+    for _ in range(4):
+        pa.copy_blocks(shape, kp, vp, kp, vp, src, dst)
+    pa.check_device_error()
+    print(f"copy pairs={num_pairs} bytes={4 * num_pairs * 32 * 16 * 128 * 2}")
+
+
 def main(argv):
     pa.load()
     torch.cuda.set_device(0)
@@ -110,6 +126,8 @@ def main(argv):
         decode_fp8(int(argv[2]) if len(argv) > 2 else 128)
     elif case == "rope":
         rope(int(argv[2]) if len(argv) > 2 else 4096)
+    elif case == "copy":
+        copy(int(argv[2]) if len(argv) > 2 else 1024)
     else:
         raise SystemExit(f"unknown case {case}")
 
