@@ -78,6 +78,30 @@ def causal_flops(prompts, prefix, Hq, d) -> float:
     return 4.0 * d * Hq * tot
 
 
+def time_each(dev, fn, iters, flush=None, warmup=3):
+    """Median device time (s) of fn() over `iters` launches, each bracketed by
+    CUDA events on the current stream, with the L2 flushed before each one
+    when `flush` (a buffer larger than L2) is given."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.add_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize(dev)
+    return float(np.median([x.elapsed_time(y) for x, y in ts])) / 1e3
+
+
+def l2_flush_buffer(dev):
+    return torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+
 # ------------------------------------------------------------------ clocks --
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
@@ -248,6 +272,10 @@ def run_ours(args, world, rank, local):
     rope = measure_rope(pa, wl, dev, hbm_peak, args.prefill_iters) if rank == 0 else None
     fp8 = measure_fp8_decode(pa, wl, dev, hbm_peak, max(20, min(args.steps, 500))) if rank == 0 else None
     serving = [measure_serving(dev, c) for c in (False, True)] if rank == 0 else None
+    long_ctx = measure_long_context(pa, wl, dev, hbm_peak, max(20, min(args.steps, 200))) if rank == 0 else None
+    mixed = measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, args.prefill_iters) if rank == 0 else None
+    churn = measure_churn(pa, wl, dev, hbm_peak, bf16_peak, args.warmup) if rank == 0 else None
+    chunked = measure_chunked_prefill(pa, wl, dev, bf16_peak, args.prefill_iters) if rank == 0 else None
 
     clocks = clk.summary()
     traffic = load_traffic("decode_splitk", nbytes, st.num_seqs)
@@ -278,6 +306,10 @@ def run_ours(args, world, rank, local):
         "rope_append": rope,
         "fp8_decode": fp8,
         "serving_loop": serving,
+        "long_context": long_ctx,
+        "mixed_step": mixed,
+        "churn": churn,
+        "chunked_prefill": chunked,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, kp, vp, st, split, args.cpu_seconds)
@@ -286,74 +318,21 @@ def run_ours(args, world, rank, local):
 
 
 def run_other_workload(args, local):
-    """Secondary measurements (not the contract line): the long-context decode
-    step (32 x 32K tokens, Hq 64 / Hkv 8) and the mixed continuous-batching
-    step (120 decode sequences + 8 prompts) through pa_mixed_step."""
+    """One secondary measurement alone (the same leg the contract line
+    carries): long_context, mixed, churn or chunked_prefill."""
     from paged_kv_cache_continuous_gb300 import binding as pa
     from paged_kv_cache_continuous_gb300 import workload as wl
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pa.load()
     hbm_peak, bf16_peak, _ = peaks()
-    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
-
-    def timed(fn, K):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(K):
-            fn()
-        b.record()
-        torch.cuda.synchronize(dev)
-        pa.check_device_error()
-        return a.elapsed_time(b) / 1e3 / K
-
-    res = {"workload": args.workload}
-    if args.workload == "long_context":
-        shape, kp, vp, st = wl.long_context(pool_device=dev)
-        q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
-        slots, bt, lens = tod(st.slot_mapping), tod(st.block_table), tod(st.seq_lens)
-        ws = pa.workspace(shape, st.num_seqs, st.max_seq_len, dev)
-        out = torch.empty_like(q)
-        split, nsplit = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
-        nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
-        t_dec = timed(lambda: pa.decode(shape, q, kp, vp, bt, lens, st.max_seq_len, out=out, ws=ws), args.steps)
-        t_app = timed(lambda: pa.kv_append(shape, kn, vn, slots, kp, vp), args.steps)
-        res.update(decode_ms=round(t_dec * 1e3, 4), decode_GBps=round(nb["decode"] / t_dec / 1e9, 1),
-                   frac_measured=round(nb["decode"] / t_dec / 1e9 / hbm_peak, 4),
-                   frac_nominal=round(nb["decode"] / t_dec / 1e9 / 8000, 4), split=split, splits=nsplit,
-                   append_ms=round(t_app * 1e3, 4))
-    else:
-        shape, kp, vp, st = wl.mixed(pool_device=dev)
-        q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
-        qs, lens, slots, bt = tod(st.q_start_loc), tod(st.seq_lens), tod(st.slot_mapping), tod(st.block_table)
-        nd = st.num_decode
-        ws = pa.workspace(shape, nd, st.max_seq_len, dev)
-        out = torch.empty_like(q)
-        step = lambda: pa.mixed_step(shape, q, kn, vn, qs, lens, slots, bt, nd, st.max_seq_len, st.max_q_len,
-                                     kp, vp, out=out, ws=ws)
-        t_step = timed(step, args.steps)
-        split, _ = pa.decode_plan(shape, nd, int(st.seq_lens[:nd].max()))
-        nb = decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)
-        n = (st.q_start_loc[nd + 1:] - st.q_start_loc[nd:-1]).tolist()
-        fl = causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim)
-        # the two halves alone, for comparison with the merged step
-        qd, btd, lensd = q[:nd], bt[:nd], lens[:nd]
-        t_dec = timed(lambda: pa.decode(shape, qd, kp, vp, btd.contiguous(), lensd.contiguous(),
-                                        int(st.seq_lens[:nd].max()), ws=ws), args.steps)
-        r0 = int(st.q_start_loc[nd])
-        qp = q[r0:].contiguous()
-        cup = (qs[nd:] - r0).contiguous()
-        btp = bt[nd:].contiguous()
-        t_pre = timed(lambda: pa.prefill(shape, qp, kp, vp, cup, st.max_q_len, block_table=btp), args.steps)
-        res.update(step_ms=round(t_step * 1e3, 4), decode_alone_ms=round(t_dec * 1e3, 4),
-                   prefill_alone_ms=round(t_pre * 1e3, 4), decode_kv_GB=round(nb["kv"] / 1e9, 4),
-                   prefill_GFLOP=round(fl / 1e9, 2), prefill_rows=int(sum(n)),
-                   decode_GBps_alone=round(nb["decode"] / t_dec / 1e9, 1),
-                   prefill_TFLOPs_alone=round(fl / t_pre / 1e12, 1))
-    print(json.dumps(res), flush=True)
+    legs = {
+        "long_context": lambda: measure_long_context(pa, wl, dev, hbm_peak, args.steps),
+        "mixed": lambda: measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, args.prefill_iters),
+        "churn": lambda: measure_churn(pa, wl, dev, hbm_peak, bf16_peak, args.warmup),
+        "chunked_prefill": lambda: measure_chunked_prefill(pa, wl, dev, bf16_peak, args.prefill_iters),
+    }
+    print(json.dumps({"workload": args.workload, **legs[args.workload]()}), flush=True)
 
 
 def load_traffic(kernel: str, nbytes, num_seqs):
@@ -458,14 +437,25 @@ def measure_copy(pa, wl, dev, hbm_peak, iters):
     t_out = timed(lambda: pa.copy_blocks(shape, kp, vp, hk, hv, src[:1024], hids))
     t_in = timed(lambda: pa.copy_blocks(shape, hk, hv, kp, vp, hids, dst[:1024]))
     fork_b, swap_b = 2 * 2 * 4096 * blk, 2 * 1024 * blk
+    # The host link's own rate: one plain pinned copy of the same bytes (both
+    # pools, 256 MB) in each direction, as a denominator for the swaps.
+    dflat, hflat = kp[:2048].view(-1), hk.view(-1)
+    hflat2 = torch.empty(2 * hflat.numel(), dtype=hflat.dtype).pin_memory()
+    t_link_out = timed(lambda: hflat2.copy_(dflat, non_blocking=True))
+    t_link_in = timed(lambda: dflat.copy_(hflat2, non_blocking=True))
+    link_out, link_in = swap_b / t_link_out / 1e9, swap_b / t_link_in / 1e9
     return {"kernel": "copy_blocks_kernel", "block_bytes_per_pool": blk,
             "fork_4096_blocks": {"ms": round(t_fork * 1e3, 4), "GBps": round(fork_b / t_fork / 1e9, 1),
                                  "frac_hbm": round(fork_b / t_fork / 1e9 / hbm_peak, 4),
                                  "bytes": "K+V read + written"},
             "swap_out_1024_blocks": {"ms": round(t_out * 1e3, 4), "GBps": round(swap_b / t_out / 1e9, 1),
-                                     "bytes": "K+V moved to pinned host"},
+                                     "bytes": "K+V moved to pinned host",
+                                     "frac_link": round(swap_b / t_out / 1e9 / link_out, 4)},
             "swap_in_1024_blocks": {"ms": round(t_in * 1e3, 4), "GBps": round(swap_b / t_in / 1e9, 1),
-                                    "bytes": "K+V moved from pinned host"}}
+                                    "bytes": "K+V moved from pinned host",
+                                    "frac_link": round(swap_b / t_in / 1e9 / link_in, 4)},
+            "link_peak": {"d2h_GBps": round(link_out, 1), "h2d_GBps": round(link_in, 1),
+                          "how": "one cudaMemcpyAsync of 256 MB between device and pinned host memory"}}
 
 
 def measure_rope(pa, wl, dev, hbm_peak, iters):
@@ -556,14 +546,181 @@ def measure_serving(dev, chunking: bool):
     for i in range(512):
         loop.submit(i, int(rng.integers(16, 513)), int(rng.integers(64, 257)))
     torch.cuda.synchronize(dev)
+    loop.time_gpu = True
     t0 = time.perf_counter()
     while loop.step() is not None:
         pass
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
+    gpu = np.array(loop.gpu_ms())
     return {"requests": 512, "steps": loop.steps, "generated_tokens": loop.generated, "wall_s": round(wall, 4),
             "tokens_per_s": round(loop.generated / wall, 1), "ms_per_step": round(wall / loop.steps * 1e3, 4),
-            "chunking": chunking}
+            "gpu_ms_per_step": round(float(gpu.mean()), 4), "gpu_s": round(float(gpu.sum()) / 1e3, 4),
+            "tokens_per_gpu_s": round(loop.generated / (float(gpu.sum()) / 1e3), 1),
+            "chunking": chunking,
+            "note": "wall clock includes host planning and Python marshalling; gpu_* is the pa_mixed_step "
+                    "device time (CUDA events) alone"}
+
+
+def measure_long_context(pa, wl, dev, hbm_peak, iters):
+    """Long-context decode: 32 sequences of 32 768 cached tokens (+1 appended),
+    Hq 64 / Hkv 8 (70B-shaped GQA), B 16: append, then split-K decode + merge.
+    The pools (4.7 GB) exceed L2, so launches run back to back."""
+    shape, kp, vp, st = wl.long_context(pool_device=dev)
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
+    q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
+    slots, bt, lens = tod(st.slot_mapping), tod(st.block_table), tod(st.seq_lens)
+    ws = pa.workspace(shape, st.num_seqs, st.max_seq_len, dev)
+    out = torch.empty_like(q)
+    split, nsplit = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
+    nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
+    t_app = time_each(dev, lambda: pa.kv_append(shape, kn, vn, slots, kp, vp), iters)
+    t_dec = time_each(dev, lambda: pa.decode(shape, q, kp, vp, bt, lens, st.max_seq_len, out=out, ws=ws), iters)
+    pa.check_device_error()
+    del kp, vp
+    return {"workload": "32 x 32768 cached tokens (+1), Hq 64 / Hkv 8, d 128, B 16",
+            "kernel": "decode_splitk_kernel + decode_merge_kernel", "split_tokens": split, "splits": nsplit,
+            "decode_ms": round(t_dec * 1e3, 5), "algorithmic_bytes": nb["decode"],
+            "GBps": round(nb["decode"] / t_dec / 1e9, 1), "frac_hbm": round(nb["decode"] / t_dec / 1e9 / hbm_peak, 4),
+            "append_ms": round(t_app * 1e3, 5), "l2": "inputs larger than L2 (pools 4.7 GB); no flush"}
+
+
+def measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, iters):
+    """The mixed continuous-batching step: 120 decode sequences (context
+    U[1,2048]) + 8 prompts U[64,1024] (sum <= 4096), Hq 32 / Hkv 8, d 128,
+    B 16, through one pa_mixed_step (append, then decode and prefill on two
+    streams); decode and prefill alone beside it.  L2 flushed before each
+    launch.  frac: the step's lower bound with decode (and append) on HBM
+    and prefill on the tensor cores perfectly overlapped, over its time."""
+    shape, kp, vp, st = wl.mixed(pool_device=dev)
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
+    q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
+    qs, lens, slots, bt = tod(st.q_start_loc), tod(st.seq_lens), tod(st.slot_mapping), tod(st.block_table)
+    nd = st.num_decode
+    ws = pa.workspace(shape, nd, st.max_seq_len, dev)
+    out = torch.empty_like(q)
+    flush = l2_flush_buffer(dev)
+    t_step = time_each(dev, lambda: pa.mixed_step(shape, q, kn, vn, qs, lens, slots, bt, nd, st.max_seq_len,
+                                                  st.max_q_len, kp, vp, out=out, ws=ws), iters, flush)
+    dmax = int(st.seq_lens[:nd].max())
+    qd, btd, lensd = q[:nd], bt[:nd].contiguous(), lens[:nd].contiguous()
+    outd = torch.empty_like(qd)
+    t_dec = time_each(dev, lambda: pa.decode(shape, qd, kp, vp, btd, lensd, dmax, out=outd, ws=ws), iters, flush)
+    r0 = int(st.q_start_loc[nd])
+    qp = q[r0:].contiguous()
+    cup = (qs[nd:] - r0).contiguous()
+    btp = bt[nd:].contiguous()
+    outp = torch.empty_like(qp)
+    t_pre = time_each(dev, lambda: pa.prefill(shape, qp, kp, vp, cup, st.max_q_len, block_table=btp, out=outp),
+                      iters, flush)
+    pa.check_device_error()
+    split, _ = pa.decode_plan(shape, nd, dmax)
+    nb = decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)
+    T = int(st.q_start_loc[-1])
+    append_b = T * shape.num_kv_heads * shape.head_dim * 2 * 2 * 2 + 4 * T
+    n = np.diff(st.q_start_loc[nd:]).tolist()
+    fl = causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim)
+    bound = max((nb["decode"] + append_b) / (hbm_peak * 1e9), fl / (bf16_peak * 1e12))
+    del kp, vp
+    return {"workload": "120 decode (context U[1,2048]) + 8 prompts U[64,1024] (sum <= 4096), Hq 32 / Hkv 8, "
+                        "d 128, B 16", "prompts": n,
+            "step_ms": round(t_step * 1e3, 5), "decode_alone_ms": round(t_dec * 1e3, 5),
+            "prefill_alone_ms": round(t_pre * 1e3, 5),
+            "decode_bytes": nb["decode"], "append_bytes": append_b, "prefill_flops": fl,
+            "decode_alone_GBps": round(nb["decode"] / t_dec / 1e9, 1),
+            "decode_alone_frac_hbm": round(nb["decode"] / t_dec / 1e9 / hbm_peak, 4),
+            "prefill_alone_tflops": round(fl / t_pre / 1e12, 1),
+            "prefill_alone_frac_bf16": round(fl / t_pre / 1e12 / bf16_peak, 4),
+            "step_bound_ms": round(bound * 1e3, 5), "frac": round(bound / t_step, 4),
+            "l2": "flushed (256 MB write) before each launch"}
+
+
+def measure_churn(pa, wl, dev, hbm_peak, bf16_peak, warmup):
+    """Fragmented serving stress: 512 sequences (log-uniform context in
+    [1, 8192]), Hq 32 / Hkv 8, d 128, B 32, 64 consecutive pa_mixed_step
+    calls; after every step a seeded 10 % finish and their blocks are reused
+    by as many prompts U[16,512], prefilled in the next step.  The index trace
+    (lengths, tables, slots) is the one the parity test checks; the rows are
+    drawn on the device.  Each step timed with CUDA events; the pools (2.3 GB)
+    exceed L2."""
+    ch = wl.Churn(pool_device=dev, draw_values=False)
+    shape = ch.shape
+    steps = [ch.step() for _ in range(ch.steps)]
+    kp, vp = ch.initial_pool()
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    Tmax = max(int(st.q_start_loc[-1]) for st in steps)
+    g = torch.Generator(device=dev).manual_seed(55)
+    rows = lambda h: torch.randn(Tmax, h, shape.head_dim, generator=g, device=dev).to(torch.bfloat16)
+    qb, kb, vb = rows(shape.num_q_heads), rows(shape.num_kv_heads), rows(shape.num_kv_heads)
+    outb = torch.empty_like(qb)
+    ws = pa.workspace(shape, 512, 8192 + 80, dev)
+    dev_steps = []
+    bytes_dec, flops_pre, rows_pre = [], [], []
+    for st in steps:
+        T, nd = int(st.q_start_loc[-1]), st.num_decode
+        rows_n = np.diff(st.q_start_loc)
+        dev_steps.append((T, nd, tod(st.q_start_loc), tod(st.seq_lens), tod(st.slot_mapping), tod(st.block_table),
+                          int(st.seq_lens.max()), int(rows_n[nd:].max()) if len(rows_n) > nd else 1))
+        split, _ = pa.decode_plan(shape, nd, int(st.seq_lens[:nd].max()))
+        bytes_dec.append(decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)["decode"]
+                         + T * shape.num_kv_heads * shape.head_dim * 8 + 4 * T)
+        n = rows_n[nd:].tolist()
+        flops_pre.append(causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim))
+        rows_pre.append(int(sum(n)))
+
+    def run(i):
+        T, nd, qs, lens, slots, bt, ml, mq = dev_steps[i]
+        pa.mixed_step(shape, qb[:T], kb[:T], vb[:T], qs, lens, slots, bt, nd, ml, mq, kp, vp, out=outb[:T], ws=ws)
+
+    for i in range(max(3, warmup)):
+        run(i % len(dev_steps))
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dev_steps]
+    for i in range(len(dev_steps)):
+        ev[i][0].record()
+        run(i)
+        ev[i][1].record()
+    torch.cuda.synchronize(dev)
+    pa.check_device_error()
+    t = np.array([a.elapsed_time(b) for a, b in ev]) / 1e3
+    bound = np.maximum(np.array(bytes_dec) / (hbm_peak * 1e9), np.array(flops_pre) / (bf16_peak * 1e12))
+    del kp, vp
+    return {"workload": "512 seqs, log-uniform context [1,8192], Hq 32 / Hkv 8, d 128, B 32, 64 steps, 10 % "
+                        "replaced per step by prompts U[16,512]",
+            "steps": len(t), "step_ms_mean": round(float(t.mean()) * 1e3, 5),
+            "step_ms_p10_p90": [round(float(np.percentile(t, 10)) * 1e3, 5), round(float(np.percentile(t, 90)) * 1e3, 5)],
+            "decode_append_GB_per_step": round(float(np.mean(bytes_dec)) / 1e9, 4),
+            "prefill_rows_per_step": round(float(np.mean(rows_pre)), 1),
+            "prefill_GFLOP_per_step": round(float(np.mean(flops_pre)) / 1e9, 2),
+            "kv_GBps": round(float(np.sum(bytes_dec) / t.sum()) / 1e9, 1),
+            "prefill_tflops": round(float(np.sum(flops_pre) / t.sum()) / 1e12, 1),
+            "step_bound_ms_mean": round(float(bound.mean()) * 1e3, 5),
+            "frac": round(float(bound.sum() / t.sum()), 4),
+            "l2": "inputs larger than L2 (pools 2.3 GB); no flush"}
+
+
+def measure_chunked_prefill(pa, wl, dev, bf16_peak, iters):
+    """Chunked prefill over a cached prefix: 4 sequences, each with 3072
+    tokens in the pool and its next 1024-token chunk (bottom-right causal),
+    Hq 32 / Hkv 8, d 128, B 16, through pa_prefill with prefix_lens.  FLOPs
+    over the unmasked pairs (prefix keys and the chunk's causal triangle)."""
+    shape, kp, vp, st, pre = wl.chunked_prefill(pool_device=dev)
+    tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
+    q, kn, vn = tod(st.q), tod(st.k_new), tod(st.v_new)
+    pa.kv_append(shape, kn, vn, tod(st.slot_mapping), kp, vp)
+    cu, bt, pl = tod(st.q_start_loc), tod(st.block_table), tod(pre)
+    out = torch.empty_like(q)
+    flush = l2_flush_buffer(dev)
+    t = time_each(dev, lambda: pa.prefill(shape, q, kp, vp, cu, st.max_q_len, prefix_lens=pl, block_table=bt,
+                                          out=out), iters, flush)
+    pa.check_device_error()
+    n = np.diff(st.q_start_loc).tolist()
+    fl = causal_flops(n, pre.tolist(), shape.num_q_heads, shape.head_dim)
+    del kp, vp
+    return {"workload": "4 x (3072 cached + 1024 new rows), Hq 32 / Hkv 8, d 128, B 16",
+            "kernel": "prefill_pair_kernel", "ms": round(t * 1e3, 5), "flops": fl,
+            "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / bf16_peak, 4),
+            "l2": "flushed (256 MB write) before each launch"}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -604,9 +761,22 @@ def cpu_baseline(shape, kp, vp, st, split, seconds):
         oracle_step(oracle, shape, kp_h, vp_h, st, seqs, threads)
         reps += 1
         t = time.perf_counter() - t0
-    return {"value": round(b * reps / t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{reps} x (append + decode of the first {len(seqs)} of {st.num_seqs} sequences, "
-                      f"{int(st.seq_lens[seqs].sum())} context tokens), fp64, {t:.1f} s"}
+    res = {"value": round(b * reps / t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"{reps} x (append + decode of the first {len(seqs)} of {st.num_seqs} sequences, "
+                     f"{int(st.seq_lens[seqs].sum())} context tokens), fp64, {t:.1f} s"}
+    # The same oracle on one thread, on a sample sized to about half the budget.
+    seqs1 = cpu_sample(st, seconds / 2, per_tok * threads)
+    b1 = decode_step_bytes(shape, st.seq_lens[seqs1], split, shape.block_size)["step"]
+    reps1, t1 = 0, 0.0
+    t0 = time.perf_counter()
+    while reps1 == 0 or t1 < seconds / 2:
+        oracle_step(oracle, shape, kp_h, vp_h, st, seqs1, 1)
+        reps1 += 1
+        t1 = time.perf_counter() - t0
+    res["single_thread"] = {"value": round(b1 * reps1 / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"{reps1} x (append + decode of the first {len(seqs1)} sequences, "
+                                      f"{int(st.seq_lens[seqs1].sum())} context tokens), fp64, {t1:.1f} s"}
+    return res
 
 
 # --------------------------------------------------------- reference arm --
@@ -655,7 +825,8 @@ def main():
     ap.add_argument("--prefill-iters", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["llama7b_decode", "long_context", "mixed"], default="llama7b_decode",
+    ap.add_argument("--workload", choices=["llama7b_decode", "long_context", "mixed", "churn", "chunked_prefill"],
+                    default="llama7b_decode",
                     help="llama7b_decode prints the contract line; the others print secondary measurements")
     args = ap.parse_args()
     if args.warmup < 3:

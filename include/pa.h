@@ -31,8 +31,16 @@
  * ---------------------------------------------------------------------------
  *  - Pointers named q, k*, v*, out, *_pool, workspace and every int32 index
  *    array are DEVICE pointers; the caller owns all of them.  The library
- *    allocates nothing and keeps no state beyond the validation flag, the
- *    decode split override and a thread-local error message.
+ *    calls no cudaMalloc.  The state it does keep, all process-wide:
+ *      - the validation flag, the decode split override and the prefill
+ *        CTA-pair override (pa_set_validation, pa_set_decode_split,
+ *        pa_set_prefill_pairs);
+ *      - a thread-local message for the last error;
+ *      - per device, created on first use and held until exit: the device
+ *        error word and the split-K scratch of pa_decode_noalloc (static
+ *        device arrays of the library, 4 bytes and 16 MiB), the side stream
+ *        and its two events that pa_mixed_step forks its prefill onto, and
+ *        the kernels' shared-memory opt-ins.
  *  - bf16 everywhere for q, k, v, pools and out; indices are int32.
  *  - Layouts (row-major, contiguous):
  *        q        [T][Hq][d]            packed query rows
@@ -188,9 +196,14 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
  *  - The first call on a device looks up that device's copy of the buffer
  *    (cudaGetSymbolAddress, with the device current); make that first call
  *    before any stream capture.
- *  - A batch whose partials need more than the buffer holds
- *    (pa_workspace_size(shape, num_seqs, max_seq_len) bytes) is rejected
+ *  - A batch whose partials need more than the buffer holds is rejected
  *    with PA_ERR_WORKSPACE before anything is enqueued; use pa_decode then.
+ *    The exact need is num_seqs * Hq * max_splits * (d + 2) * 4 bytes, with
+ *    max_splits from pa_decode_plan(shape, num_seqs, max_seq_len) (0 bytes
+ *    when max_splits is 1).  pa_workspace_size(shape, num_seqs, max_seq_len)
+ *    is an upper bound of that need (it assumes the shortest split), so a
+ *    batch with pa_workspace_size <= PA_NOALLOC_SCRATCH_BYTES is always
+ *    accepted, and larger ones often are.
  *  - All calls share the one buffer and nothing in it needs clearing (every
  *    partial is written before it is read); calls whose kernels overlap on
  *    the GPU (different streams, no ordering) race on it.

@@ -8,12 +8,21 @@ a prefill; max_waiting_tokens forces admission after that many steps;
 waiting_served_ratio sets the least batch worth admitting, running size x
 ratio; with prefill chunking both are ignored and new prompts are prefilled
 together with the running batch's step), with the launcher defaults of the
-TGI architecture wiki, section "Router".  Where the pages are silent, the
-readings are the library's documented ones (one step = decode of every
-running request plus the step's prefill rows; reservations block-aligned
-prompt + max_new; strict FIFO; chunks within max_batch_prefill_tokens minus
-the decode rows, prompts under way first; first token at the end of the
-prompt, leave after max_new tokens).
+TGI architecture wiki, section "Router".  Where the page is silent, this
+reference takes the plainest reading of the loop it describes, each stated
+here and nowhere derived from the code under test:
+  - one step is one forward pass: every running request whose prompt is done
+    decodes one token, and the step's admitted prompt rows are prefilled in
+    the same pass (the page prefills new prompts with the running batch);
+  - a request's reservation against the total-token budget is its prompt
+    plus its max_new tokens, rounded up to whole blocks (the router's block
+    allocator hands out whole blocks, TGI architecture wiki, "Router");
+  - the queue is FIFO: admission takes requests in arrival order and stops
+    at the first that does not fit (no request overtakes another);
+  - with chunking, a step's prefill rows plus its decode rows stay within
+    max_batch_prefill_tokens, and prompts already under way go first;
+  - a request's first token comes at the end of its prompt, and it leaves
+    once it has produced max_new tokens.
 
 Plain Python: lists, dicts and integer arithmetic, step by step.  Block ids
 are not modelled (only counts): where several block assignments are valid,

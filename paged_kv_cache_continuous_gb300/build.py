@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 print(o, file=sys.stderr)
     tmp = BUILD / f"libpagedattn.{os.getpid()}.so"
     objs = [str(BUILD / (s + ".o")) for s in CU_SOURCES + CXX_SOURCES]
-    _run([nv, *ARCH, "-shared", "-o", str(tmp), *objs])
+    _run([nv, *ARCH, "-shared", "-o", str(tmp), *objs, "-ldl"])
     os.replace(tmp, LIB)
     return LIB
 

@@ -461,14 +461,10 @@ template <int D, int BS, bool BIG_G, bool FP8>
 cudaError_t launch_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                             cudaStream_t stream) {
     using C = DecodeCfg<D, BS, FP8>;
-    static bool attr_set = false;  // benign race: the attribute call is idempotent
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitk_kernel<D, BS, BIG_G, FP8>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> opted{0};
+    cudaError_t e0 = opt_in_smem(reinterpret_cast<const void *>(decode_splitk_kernel<D, BS, BIG_G, FP8>),
+                                 C::kSmemBytes, opted);
+    if (e0 != cudaSuccess) return e0;
     dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
     decode_splitk_kernel<D, BS, BIG_G, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_k, tm_v, a);
     cudaError_t e = cudaGetLastError();

@@ -11,12 +11,25 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pa.h"
 #include "pa_internal.h"
 
 namespace {
 
 using namespace pa;
+
+// A named NVTX range around each public call that enqueues GPU work, so a
+// profiler's timeline shows which library call launched which kernels (free
+// when no tool is attached: NVTX is header-only and calls into a tool only
+// when one is injected).
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
 
 thread_local std::string t_last_error;
 std::atomic<int> g_validation{0};
@@ -187,10 +200,14 @@ int do_append(const pa_shape_t *sh, const void *k_new, const void *v_new, const 
 int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const void *v_pool,
               const int32_t *block_table, int max_blocks, const int32_t *seq_lens, int num_seqs,
               int max_seq_len, void *out, void *ws, size_t ws_bytes, cudaStream_t st, DevState *d,
-              int check_first, const float *k_scale = nullptr, const float *v_scale = nullptr) {
+              int check_first, const float *k_scale = nullptr, const float *v_scale = nullptr,
+              int split_planned = 0) {
     const bool fp8 = k_scale != nullptr;
-    const int split = decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len, sh->block_size,
-                                          d->num_sms, g_split_override.load());
+    // split_planned > 0: the caller has already planned the split (and sized
+    // its scratch from it); the override is not read a second time.
+    const int split = split_planned > 0 ? split_planned
+                                        : decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len,
+                                                              sh->block_size, d->num_sms, g_split_override.load());
     const int max_splits = decode_max_splits(max_seq_len, split);
     const size_t need = decode_workspace_bytes(num_seqs, sh->num_q_heads, sh->head_dim, max_splits);
     if (need > 0 && (ws == nullptr || ws_bytes < need))
@@ -372,6 +389,7 @@ int pa_decode_plan(const pa_shape_t *shape, int num_seqs, int max_seq_len, int *
 
 int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new, const int32_t *slot_mapping,
                  int num_tokens, void *k_pool, void *v_pool, void *stream) {
+    Range range_("pa_kv_append");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
@@ -400,6 +418,7 @@ int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new, 
 int pa_rope_append(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
                    const int32_t *positions, const int32_t *slot_mapping, int num_tokens, float rope_theta,
                    void *q_out, void *k_pool, void *v_pool, void *stream) {
+    Range range_("pa_rope_append");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
@@ -450,6 +469,7 @@ int pa_rope_append(const pa_shape_t *shape, const void *q, const void *k_new, co
 int pa_copy_blocks(const pa_shape_t *shape, const void *src_k, const void *src_v, int src_num_blocks,
                    void *dst_k, void *dst_v, int dst_num_blocks, const int32_t *src_ids,
                    const int32_t *dst_ids, int num_pairs, void *stream) {
+    Range range_("pa_copy_blocks");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
@@ -486,6 +506,7 @@ int pa_copy_blocks(const pa_shape_t *shape, const void *src_k, const void *src_v
 int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
               const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
               int max_seq_len, void *out, void *workspace, size_t ws_bytes, void *stream) {
+    Range range_("pa_decode");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
@@ -523,6 +544,7 @@ int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const 
 int pa_kv_append_fp8(const pa_shape_t *shape, const void *k_new, const void *v_new, const int32_t *slot_mapping,
                      int num_tokens, const float *k_scale, const float *v_scale, void *k_pool, void *v_pool,
                      void *stream) {
+    Range range_("pa_kv_append_fp8");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
@@ -557,6 +579,7 @@ int pa_decode_fp8(const pa_shape_t *shape, const void *q, const void *k_pool, co
                   const float *k_scale, const float *v_scale, const int32_t *block_table, int max_blocks_per_seq,
                   const int32_t *seq_lens, int num_seqs, int max_seq_len, void *out, void *workspace,
                   size_t ws_bytes, void *stream) {
+    Range range_("pa_decode_fp8");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (shape->head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "fp8 decode supports head_dim 128");
@@ -595,6 +618,7 @@ int pa_decode_fp8(const pa_shape_t *shape, const void *q, const void *k_pool, co
 int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool, const void *v_pool,
                       const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
                       int max_seq_len, void *out, void *stream) {
+    Range range_("pa_decode_noalloc");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
@@ -635,7 +659,7 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
         if ((rc = run_check(ca, st))) return rc;
     }
     rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
-                   out, scratch, PA_NOALLOC_SCRATCH_BYTES, st, d, val);
+                   out, scratch, PA_NOALLOC_SCRATCH_BYTES, st, d, val, nullptr, nullptr, split);
     if (rc) return rc;
     return ok();
 }
@@ -643,6 +667,7 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
 int pa_prefill(const pa_shape_t *shape, const void *q, const void *k, const void *v, const int32_t *cu_seqlens_q,
                const int32_t *prefix_lens, const int32_t *block_table, int max_blocks_per_seq, int num_seqs,
                int num_tokens, int max_q_len, void *out, void *stream) {
+    Range range_("pa_prefill");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_seqs < 0 || num_tokens < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
@@ -685,6 +710,7 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
                   const int32_t *block_table, int max_blocks_per_seq, int num_seqs, int num_decode,
                   int num_tokens, int max_seq_len, int max_q_len, void *k_pool, void *v_pool, void *out,
                   void *workspace, size_t ws_bytes, void *stream) {
+    Range range_("pa_mixed_step");
     int rc = check_shape(shape);
     if (rc) return rc;
     if (num_seqs < 0 || num_decode < 0 || num_decode > num_seqs || num_tokens < 0 || max_seq_len < 0 ||
@@ -776,6 +802,7 @@ int pa_set_prefill_pairs(int pairs) {
 }
 
 int pa_check_device_error(void *stream) {
+    Range range_("pa_check_device_error");
     DevState *d;
     int rc = dev_state(&d);
     if (rc) return rc;

@@ -6,7 +6,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace pa {
+
+// Dynamic shared memory above 48 KB needs an opt-in per kernel and per
+// device (function attributes belong to the device's context).  `done` holds
+// one bit per device ordinal (< 64) already opted in; a higher ordinal is
+// set on every launch.  Concurrent first launches may both set the attribute,
+// which is idempotent.
+inline cudaError_t opt_in_smem(const void *kernel, int bytes, std::atomic<unsigned long long> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // ------------------------------------------------------------- decode ------
 struct DecodeArgs {

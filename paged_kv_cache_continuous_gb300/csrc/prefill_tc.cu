@@ -411,13 +411,10 @@ template <int D, int BS, bool PAGED, bool HEAD_PAIR>
 cudaError_t launch_prefill_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const PrefillArgs &a, cudaStream_t stream) {
     using C = PrefillCfg<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BS, PAGED, HEAD_PAIR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> opted{0};
+    cudaError_t e0 = opt_in_smem(reinterpret_cast<const void *>(prefill_tc_kernel<D, BS, PAGED, HEAD_PAIR>),
+                                 C::kSmemBytes, opted);
+    if (e0 != cudaSuccess) return e0;
     dim3 grid(HEAD_PAIR ? a.num_q_tiles : (a.num_q_tiles + 1) / 2,
               HEAD_PAIR ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
     prefill_tc_kernel<D, BS, PAGED, HEAD_PAIR><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, a);

@@ -814,13 +814,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <int BS, bool PAGED, int MODE>
 cudaError_t launch_pair_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const CUtensorMap &tm_o, const PrefillArgs &a, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<BS, PAGED, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> opted{0};
+    cudaError_t e0 = opt_in_smem(reinterpret_cast<const void *>(prefill_pair_kernel<BS, PAGED, MODE>), kSmemBytes,
+                                 opted);
+    if (e0 != cudaSuccess) return e0;
     const long long units = (long long)((a.num_q_tiles + per_pair(MODE) - 1) / per_pair(MODE)) *
                             (a.num_q_heads / heads_per_pair(MODE)) * a.num_seqs;
     if (units == 0) return cudaSuccess;

@@ -33,6 +33,8 @@ class ServingLoop:
         self.finished = []
         self.prompt_len = {}
         self.last = None  # the last step's inputs (host numpy / device tensors), for checking
+        self.gpu_events = []  # (start, end) CUDA events around each step's pa_mixed_step, if timed
+        self.time_gpu = False
 
     def submit(self, request_id: int, input_tokens: int, max_new_tokens: int):
         self.sched.submit(request_id, input_tokens, max_new_tokens)
@@ -59,7 +61,13 @@ class ServingLoop:
         max_len = int(plan["seq_lens"].max())
         if keep_inputs:
             self.last = dict(plan=plan, q=q, k=kn, v=vn, kp_before=self.kp.clone(), vp_before=self.vp.clone())
+        if self.time_gpu:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record()
         out = pa.mixed_step(sh, q, kn, vn, qs, lens, slots, bt, nd, max_len, max_q, self.kp, self.vp)
+        if self.time_gpu:
+            ev[1].record()
+            self.gpu_events.append(ev)
         if keep_inputs:
             self.last["out"] = out
         done = self.sched.commit()
@@ -71,3 +79,8 @@ class ServingLoop:
         for rid in done:
             self.prompt_len.pop(rid, None)
         return plan
+
+    def gpu_ms(self) -> list[float]:
+        """Device time of each timed step's pa_mixed_step (synchronises)."""
+        torch.cuda.synchronize(self.device)
+        return [a.elapsed_time(b) for a, b in self.gpu_events]

@@ -152,12 +152,16 @@ def new_pool(shape: Shape, seed: int, device="cpu"):
 
 def make_step(alloc: BlockAllocator, shape: Shape, seqs, n_new, total_after,
               num_decode: int, gen: torch.Generator, width: int | None = None,
-              stale_fill: int = -1, stale_gen: np.random.Generator | None = None) -> Step:
+              stale_fill: int = -1, stale_gen: np.random.Generator | None = None,
+              value_gen: torch.Generator | None = None, draw_values: bool = True) -> Step:
     """Reserve blocks and draw q/k_new/v_new for one step.
 
     seqs[i] gets n_new[i] new tokens at positions total_after[i]-n_new[i] ..
     total_after[i]-1.  Block-table entries past a sequence's last block are
-    ``stale_fill`` (or seeded junk when ``stale_gen`` is given)."""
+    ``stale_fill`` (or seeded junk when ``stale_gen`` is given).  The values
+    come from ``value_gen`` (default ``gen``); with ``draw_values=False`` they
+    are not drawn (q/k_new/v_new are None: index-only use, e.g. when the
+    values are drawn on the device)."""
     n_new = [int(n) for n in n_new]
     total_after = [int(t) for t in total_after]
     for s, L in zip(seqs, total_after):
@@ -178,9 +182,12 @@ def make_step(alloc: BlockAllocator, shape: Shape, seqs, n_new, total_after,
             used = -(-L // B)
             junk = stale_gen.integers(-(2 ** 31), 2 ** 31 - 1, size=width - used, dtype=np.int64)
             bt[r, used:] = junk.astype(np.int32)
-    q = bf16_randn((T, shape.num_q_heads, shape.head_dim), gen)
-    k = bf16_randn((T, shape.num_kv_heads, shape.head_dim), gen)
-    v = bf16_randn((T, shape.num_kv_heads, shape.head_dim), gen)
+    q = k = v = None
+    if draw_values:
+        vg = gen if value_gen is None else value_gen
+        q = bf16_randn((T, shape.num_q_heads, shape.head_dim), vg)
+        k = bf16_randn((T, shape.num_kv_heads, shape.head_dim), vg)
+        v = bf16_randn((T, shape.num_kv_heads, shape.head_dim), vg)
     return Step(shape=shape, q=q, k_new=k, v_new=v, q_start_loc=q_start,
                 seq_lens=np.asarray(total_after, dtype=np.int32), slot_mapping=slots,
                 block_table=bt, num_decode=int(num_decode), seq_ids=list(seqs))
@@ -293,6 +300,23 @@ def prefill_only(seed: int, prompts, num_q_heads=32, num_kv_heads=8, head_dim=12
     return shape, kp, vp, step
 
 
+def chunked_prefill(seed: int = 6, num_seqs: int = 4, prefix: int = 3072, chunk: int = 1024,
+                    num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, pool_device="cpu"):
+    """Chunked prefill over a cached prefix: each sequence already holds
+    ``prefix`` tokens in the pool (initial contents) and brings its next
+    ``chunk`` prompt rows, appended at positions prefix .. prefix + chunk - 1.
+    Returns (shape, k_pool, v_pool, step, prefix_lens)."""
+    g = torch.Generator().manual_seed(seed)
+    L = prefix + chunk
+    N = math.ceil(1.1 * num_seqs * -(-L // block_size))
+    shape = Shape(num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                  block_size=block_size, num_blocks=N)
+    alloc = BlockAllocator(N, block_size, _permutation(N, g))
+    step = make_step(alloc, shape, list(range(num_seqs)), [chunk] * num_seqs, [L] * num_seqs, 0, g)
+    kp, vp = new_pool(shape, seed * 1000 + 7, pool_device)
+    return shape, kp, vp, step, np.full(num_seqs, prefix, dtype=np.int32)
+
+
 def log_uniform_context(g: torch.Generator, n: int, hi: int = 8192) -> list[int]:
     """L = clamp(floor(exp(U(0, ln(hi + 1)))), 1, hi)."""
     u = torch.rand(n, generator=g, dtype=torch.float64)
@@ -304,13 +328,19 @@ class Churn:
     [1, 8192], B = 32), 64 steps.  Every step each running sequence decodes
     one token; after the step round(0.1 * S) sequences finish (sampled without
     replacement), their blocks go back on the free list, and as many new
-    prompts U[16, 512] join the next step as prefills."""
+    prompts U[16, 512] join the next step as prefills.
+
+    Lengths, block assignment and finishing are drawn from one generator and
+    the step's q/k/v rows from a second (seed + 1), so ``draw_values=False``
+    gives the same trace of indices without drawing the values."""
 
     def __init__(self, seed: int = 5, num_seqs: int = 512, steps: int = 64,
                  max_context: int = 8192, prompt_range=(16, 512), finish_frac: float = 0.1,
                  pool_device="cpu", num_q_heads=32, num_kv_heads=8, head_dim=128,
-                 block_size=32):
+                 block_size=32, draw_values: bool = True):
         self.g = torch.Generator().manual_seed(seed)
+        self.gv = torch.Generator().manual_seed(seed + 1)
+        self.draw_values = draw_values
         self.steps = steps
         self.prompt_range = prompt_range
         self.num_finish = int(round(finish_frac * num_seqs))
@@ -343,7 +373,7 @@ class Churn:
         n_new = [1] * len(decode_ids) + [self.prompt_len[s] for s in prompt_ids]
         after = [self.ctx[s] + 1 for s in decode_ids] + [self.prompt_len[s] for s in prompt_ids]
         st = make_step(self.alloc, self.shape, seqs, n_new, after, len(decode_ids), self.g,
-                       width=self.width)
+                       width=self.width, value_gen=self.gv, draw_values=self.draw_values)
         for s, L in zip(seqs, after):
             self.ctx[s] = L
         for s in prompt_ids:

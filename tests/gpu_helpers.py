@@ -21,30 +21,125 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers (8 significant bits) at |x| (normal
+    range): 2^(e - 8) for 2^e <= |x| < 2^(e+1)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+# Elements admitted above the 1e-2 bar, per comparison; each one is recorded
+# here and printed, never hidden.  Two readings admit an element:
+#  - large outputs: a bf16 output of magnitude >= 4 is spaced 2^-5 apart, so
+#    rounding alone can leave it up to 2^-6 > 1e-2 from the exact value; it
+#    passes within half a bf16 ulp of the oracle value plus 1e-3;
+#  - the bf16 weights' own bound, where the caller can give the softmax
+#    spread E = sum_j p_j |v_j - out| of the element (p the exact softmax
+#    weights): the kernels multiply V by weights rounded to bf16 (relative
+#    error u = 2^-8 each) and divide by the sum of those same rounded
+#    weights, so out_gpu - out = sum_j p_j e_j (v_j - out) / (1 + O(u)),
+#    at most u / (1 - u) * E, before the final rounding to bf16 adds up to
+#    half an ulp.  With V ~ N(0,1) and a few dominant keys, E reaches 2-4 and
+#    this can exceed 1e-2 for outputs of magnitude >= 2.
+LARGE_OUTPUT_EXCEPTIONS: list[dict] = []
+U_BF16 = 2.0 ** -8
+
+
+def bf16_weight_bound(ref: np.ndarray, spread: np.ndarray) -> np.ndarray:
+    """Error bound of an output computed from bf16-rounded softmax weights
+    with consistent normalisation, then rounded to bf16 (fp32 accumulation
+    slack 1e-5)."""
+    pre = U_BF16 / (1 - U_BF16) * spread
+    return pre + bf16_half_ulp(np.abs(ref) + pre) + 1e-5
+
+
 def assert_close(gpu_bf16: torch.Tensor, ref: np.ndarray, what: str = "",
-                 max_abs: float = MAX_ABS, mean_abs: float = MEAN_ABS):
+                 max_abs: float = MAX_ABS, mean_abs: float = MEAN_ABS, spread=None):
+    """Element-wise comparison with the oracle.  `spread(index) -> E`
+    (optional) gives the softmax spread of one output element (an index into
+    `ref`), for the bf16-weight bound above."""
     g = gpu_bf16.detach().float().cpu().double().numpy().reshape(ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     err = np.abs(g - ref)
-    mx, mean = float(err.max()), float(err.mean())
-    assert mx <= max_abs and mean <= mean_abs, f"{what}: max abs {mx:.3g}, mean abs {mean:.3g}"
-    return mx, mean
+    mean = float(err.mean())
+    over = err > max_abs
+    if over.any():
+        idx = np.argwhere(over)
+        r, e = ref[over], err[over]
+        admitted = (np.abs(r) >= 4.0) & (e <= bf16_half_ulp(r) + 1e-3)
+        bound = np.full(len(r), np.nan)
+        if spread is not None:
+            for i in range(len(r)):
+                bound[i] = bf16_weight_bound(np.array([r[i]]), np.array([spread(tuple(idx[i]))]))[0]
+            admitted |= e <= bound
+        for i, ok in enumerate(admitted):
+            rec = {"what": what, "index": tuple(int(x) for x in idx[i]), "oracle": float(r[i]),
+                   "gpu": float(g[tuple(idx[i])]), "err": float(e[i]), "bf16_weight_bound": float(bound[i]),
+                   "admitted": bool(ok)}
+            if ok:
+                LARGE_OUTPUT_EXCEPTIONS.append(rec)
+                print(f"element admitted above {max_abs}: {rec}")
+        assert admitted.all(), (f"{what}: {int((~admitted).sum())} elements above {max_abs}; worst "
+                                f"{float(e[~admitted].max()):.3g} at |oracle| "
+                                f"{float(np.abs(r[~admitted][np.argmax(e[~admitted])])):.3g}")
+    assert mean <= mean_abs, f"{what}: max abs {float(err.max()):.3g}, mean abs {mean:.3g}"
+    return float(err.max()), mean
 
 
-def compact_pool(k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: np.ndarray,
-                 seq_lens: np.ndarray, rows, block_size: int):
+def prefill_spread(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu: np.ndarray, ref: np.ndarray,
+                   scale: float | None = None):
+    """spread(index) for dense causal prefill outputs [T][Hq][d]: the exact
+    (fp64) softmax weights of row r over keys cu[s] .. r, and
+    sum_j p_j |v_j[c] - ref[r, h, c]|.  q/k/v are float64 arrays."""
+    d = q.shape[-1]
+    G = q.shape[1] // k.shape[1]
+    sc = 1.0 / np.sqrt(d) if scale is None else scale
+
+    def f(index):
+        r, h, c = index
+        s = int(np.searchsorted(cu, r, side="right")) - 1
+        keys = slice(int(cu[s]), r + 1)
+        x = sc * (k[keys, h // G] @ q[r, h])
+        p = np.exp(x - x.max())
+        p /= p.sum()
+        return float(p @ np.abs(v[keys, h // G, c] - ref[r, h, c]))
+    return f
+
+
+def assert_appended(k_pool: torch.Tensor, v_pool: torch.Tensor, st, block_size: int, what: str = ""):
+    """The rows a step appended, read back from the device pools at its slots,
+    equal the step's k_new / v_new bit for bit (padding slots < 0 skipped).
+    Full-size tests check this before the oracle reads the device pools, so
+    an append bug cannot pass into the reference unseen."""
+    slots = np.asarray(st.slot_mapping)
+    keep = np.nonzero(slots >= 0)[0]
+    sl = torch.tensor(slots[keep], dtype=torch.long, device=k_pool.device)
+    rows = torch.tensor(keep, dtype=torch.long)
+    blk, off = sl // block_size, sl % block_size
+    for pool, new, name in ((k_pool, st.k_new, "K"), (v_pool, st.v_new, "V")):
+        got = pool[blk, :, off, :].cpu()
+        assert torch.equal(got.view(torch.int16), new[rows].contiguous().view(torch.int16)), \
+            f"{what}: appended {name} rows differ from the step's new rows"
+
+
+def compact_pool(k_pool, v_pool, block_table: np.ndarray, seq_lens: np.ndarray, rows, block_size: int):
     """Host copies of only the blocks that sequences `rows` use, with their
     table rows renumbered to the compact pool (a block relabelling, which
-    leaves attention unchanged)."""
+    leaves attention unchanged).  The pools are device tensors or host uint16
+    arrays (the oracle's mirror)."""
     used = []
     for r in rows:
         nb = -(-int(seq_lens[r]) // block_size)
         used += block_table[r, :nb].tolist()
     uniq = sorted(set(used))
     remap = {b: i for i, b in enumerate(uniq)}
-    idx = torch.tensor(uniq if uniq else [0], dtype=torch.long, device=k_pool.device)
-    kc = bits(k_pool.index_select(0, idx))
-    vc = bits(v_pool.index_select(0, idx))
+    if isinstance(k_pool, np.ndarray):
+        idx = np.array(uniq if uniq else [0], dtype=np.int64)
+        kc, vc = np.ascontiguousarray(k_pool[idx]), np.ascontiguousarray(v_pool[idx])
+    else:
+        idx = torch.tensor(uniq if uniq else [0], dtype=torch.long, device=k_pool.device)
+        kc = bits(k_pool.index_select(0, idx))
+        vc = bits(v_pool.index_select(0, idx))
     width = block_table.shape[1]
     bt = np.full((len(rows), width), -1, dtype=np.int32)
     for i, r in enumerate(rows):

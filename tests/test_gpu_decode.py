@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_close, bits, compact_pool, dev, sample
+from gpu_helpers import assert_appended, assert_close, bits, compact_pool, dev, sample
 from paged_kv_cache_continuous_gb300 import binding as pa
 from paged_kv_cache_continuous_gb300 import workload as wl
 
@@ -165,13 +165,21 @@ def test_validation_mode_skips_work(cuda_lib):
 
 
 def _sampled_full_size(shape, kp_d, vp_d, st, rng, n_pairs, what):
+    """Full-size step: the initial pools are drawn on the device (a seeded
+    generator) and copied to the host before the GPU append; the oracle then
+    appends on that host mirror, and the whole device pool must equal it bit
+    for bit before the oracle decodes sampled (sequence, head) pairs from it."""
     kd, vd = kp_d, vp_d
+    kh, vh = bits(kd), bits(vd)
     pa.kv_append(shape, dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), kd, vd)
     out = _decode_gpu(shape, kd, vd, st)
     pa.check_device_error()
+    assert_appended(kd, vd, st, shape.block_size, what)
+    oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, kh, vh, inplace=True)
+    assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh), f"{what}: pools after the append"
     S, Hq = st.num_seqs, shape.num_q_heads
     seqs = sample(rng, S, 12)
-    kc, vc, bt = compact_pool(kd, vd, st.block_table, st.seq_lens, seqs, shape.block_size)
+    kc, vc, bt = compact_pool(kh, vh, st.block_table, st.seq_lens, seqs, shape.block_size)
     pairs = np.array([(i, int(h)) for i in range(len(seqs)) for h in rng.choice(Hq, 4, replace=False)],
                      dtype=np.int32)
     q = bits(st.q)[seqs]

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_close, bits, compact_pool, dev, sample
+from gpu_helpers import assert_appended, assert_close, bits, compact_pool, dev, prefill_spread, sample
 from paged_kv_cache_continuous_gb300 import binding as pa
 from paged_kv_cache_continuous_gb300 import workload as wl
 
@@ -48,7 +48,12 @@ def test_prefill_growing_scores(cuda_lib, slope):
     slope 1 moves every row's running maximum by ~2^130 per 128-key tile, 0.1 by
     ~2^13 (a move past 2^64 every few tiles), -0.1 keeps the first key the
     largest -- the paths where the kernel moves its running maximum and
-    rescales O."""
+    rescales O.  V ~ N(0,1) as everywhere else.  With weights halving per
+    key at slope 1, an output is dominated by a few values: its bf16 rounding
+    (up to 2^-7 for magnitudes in [2, 4), 2^-6 in [4, 8)) plus the bf16
+    rounding of the dominant weights can pass 1e-2.  Such elements are held
+    to the bound of that arithmetic (bf16 weights, consistent normalisation,
+    bf16 output) computed from their exact softmax weights, and printed."""
     g = torch.Generator().manual_seed(23)
     lens = [1000, 700, 129]
     T, Hq, Hkv, d = sum(lens), 32, 8, 128
@@ -58,16 +63,15 @@ def test_prefill_growing_scores(cuda_lib, slope):
     k = (torch.randn(T, Hkv, d, generator=g) * 0.1)
     pos = torch.cat([torch.arange(L, dtype=torch.float32) for L in lens])
     k[:, :, 0] = slope * pos[:, None]
-    # Such peaked weights (about halving per key at slope 1) magnify the bf16
-    # rounding of P; V at half the usual spread keeps that within tolerance.
-    v = torch.randn(T, Hkv, d, generator=g) * 0.5
+    v = torch.randn(T, Hkv, d, generator=g)
     q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
     cu = np.zeros(len(lens) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(lens)
     out = pa.prefill(shape, dev(q), dev(k), dev(v), dev(cu), max(lens))
     pa.check_device_error()
     ref = oracle.prefill(bits(q), bits(k), bits(v), cu)
-    assert_close(out, ref, f"growing scores slope={slope}")
+    f64 = lambda t: t.double().numpy()
+    assert_close(out, ref, f"growing scores slope={slope}", spread=prefill_spread(f64(q), f64(k), f64(v), cu, ref))
 
 
 def _paged_case(seed, prefix_and_new, Hq, Hkv, d, B):
@@ -168,15 +172,19 @@ def test_prefill_bad_block_flags_error(cuda_lib):
 def test_prefill_full_size_sampled(cuda_lib, prompts):
     shape, kp, vp, st = wl.prefill_only(40 + len(prompts), prompts, pool_device="cuda")
     kd, vd = kp, vp
+    kh, vh = bits(kd), bits(vd)  # the drawn initial pools, before the GPU append
     pa.kv_append(shape, dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), kd, vd)
     out = pa.prefill(shape, dev(st.q), kd, vd, dev(st.q_start_loc), st.max_q_len,
                      block_table=dev(st.block_table))
     pa.check_device_error()
+    assert_appended(kd, vd, st, shape.block_size, f"prefill {prompts}")
+    oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, kh, vh, inplace=True)
+    assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh), "pools after the append"
     rng = np.random.default_rng(2)
     rows = np.concatenate([sample(rng, st.num_tokens, 40), st.q_start_loc[1:] - 1, st.q_start_loc[:-1]])
     pairs = np.array([(int(r), int(h)) for r in rows for h in rng.choice(shape.num_q_heads, 3, replace=False)],
                      dtype=np.int32)
-    kc, vc, bt = compact_pool(kd, vd, st.block_table, st.seq_lens, range(st.num_seqs), shape.block_size)
+    kc, vc, bt = compact_pool(kh, vh, st.block_table, st.seq_lens, range(st.num_seqs), shape.block_size)
     ref = oracle.prefill(bits(st.q), kc, vc, st.q_start_loc, block_table=bt, pairs=pairs)
     got = out[torch.tensor(pairs[:, 0]), torch.tensor(pairs[:, 1])]
     assert_close(got, ref, f"prefill {prompts}")
