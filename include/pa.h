@@ -94,10 +94,13 @@ typedef struct {
 int pa_version(void);
 
 /*
- * Workspace bytes needed by pa_decode / pa_mixed_step for batches of at most
- * max_seqs sequences whose lengths (after the step's append) are at most
- * max_seq_len.  The workspace holds split-K partial results (fp32) and is
- * owned by the caller; its contents need no initialisation.  Writes *bytes.
+ * Workspace bytes needed by pa_decode / pa_decode_append / pa_decode_fp8 /
+ * pa_mixed_step for batches of at most max_seqs sequences whose lengths
+ * (after the step's append) are at most max_seq_len.  The workspace holds the
+ * decode plan (the batch's work items, one per sequence, KV head and split,
+ * and two counters) and the split-K partial results (fp32); it is owned by
+ * the caller, its contents need no initialisation, and two calls whose
+ * kernels may overlap on the GPU need two workspaces.  Writes *bytes.
  */
 int pa_workspace_size(const pa_shape_t *shape, int max_seqs, int max_seq_len,
                       size_t *bytes);
@@ -141,6 +144,31 @@ int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool,
               void *stream);
 
 /*
+ * Decode step with its append fused in: the same result as
+ *     pa_kv_append(k_new, v_new, slot_mapping, num_seqs rows)
+ *     followed by pa_decode(...)
+ * in one launch (plus the merge).  Sequence s brings one new row,
+ * k_new[s] / v_new[s] ([S][Hkv][d]), whose slot is slot_mapping[s] (< 0:
+ * none); the CTA that reads the sequence's last block writes the row there
+ * first and orders that write before its own read of the block, so the row
+ * is attended to without a separate pass over the new rows (the pages' decode
+ * step: the new token's key and value join the cache and the new token
+ * attends to all of it, text-generation-inference Router/Webserver deep
+ * dive, section "Prefill, Decode and past key values").
+ * Requirement (the router's allocator meets it): slot_mapping[s] >= 0 is the
+ * slot of position seq_lens[s] - 1 of sequence s, i.e.
+ * block_table[s][(L-1)/B] * B + (L-1) % B; in validation mode any other
+ * slot sets PA_ERR_BAD_INDEX and nothing is written.  A slot past the pool
+ * sets the error word and is skipped.  Arguments, workspace, errors and
+ * asynchrony as pa_decode and pa_kv_append; bf16 pools only.
+ */
+int pa_decode_append(const pa_shape_t *shape, const void *q, const void *k_new,
+                     const void *v_new, const int32_t *slot_mapping, void *k_pool,
+                     void *v_pool, const int32_t *block_table, int max_blocks_per_seq,
+                     const int32_t *seq_lens, int num_seqs, int max_seq_len, void *out,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Causal prefill over packed prompts: rows [cu_seqlens_q[s], cu_seqlens_q[s+1])
  * of q belong to sequence s.  Row i of sequence s sits at absolute position
  * p0 + i and attends to keys 0 .. p0 + i (bottom-right causal alignment).
@@ -168,10 +196,14 @@ int pa_prefill(const pa_shape_t *shape, const void *q, const void *k,
  *      query row each (q_start_loc[s+1] - q_start_loc[s] == 1);
  *   3. causal prefill (paged form, prefix = seq_lens[s] - n_s) for sequences
  *      [num_decode, num_seqs).
- * Steps 2 and 3 run concurrently: the prefill goes to a higher-priority
- * stream owned by the library (one per device, created on first use), forked
- * from `stream` after the append and joined back into it with events, so work
- * enqueued on `stream` afterwards sees the whole step.
+ * Steps 2 and 3 run concurrently: the decode rows' append is fused into the
+ * decode kernel (as pa_decode_append, so each decode row's slot must be its
+ * sequence's last position), which starts at once on `stream`; the prompt
+ * rows' append and the prefill go to a higher-priority stream owned by the
+ * library (one per device, created on first use), forked from `stream` and
+ * joined back into it with events, so work enqueued on `stream` afterwards
+ * sees the whole step.  Blocks that one sequence writes in the step must not
+ * be read by another (the allocator's ownership rule).
  * q_start_loc [num_seqs+1] packs the rows of q/k_new/v_new/out; seq_lens counts
  * tokens after the append.  max_seq_len bounds seq_lens, max_q_len bounds the
  * prefill rows per sequence.  workspace as for pa_decode.
@@ -198,12 +230,13 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
  *    before any stream capture.
  *  - A batch whose partials need more than the buffer holds is rejected
  *    with PA_ERR_WORKSPACE before anything is enqueued; use pa_decode then.
- *    The exact need is num_seqs * Hq * max_splits * (d + 2) * 4 bytes, with
- *    max_splits from pa_decode_plan(shape, num_seqs, max_seq_len) (0 bytes
- *    when max_splits is 1).  pa_workspace_size(shape, num_seqs, max_seq_len)
- *    is an upper bound of that need (it assumes the shortest split), so a
- *    batch with pa_workspace_size <= PA_NOALLOC_SCRATCH_BYTES is always
- *    accepted, and larger ones often are.
+ *    The exact need, with max_splits from pa_decode_plan(shape, num_seqs,
+ *    max_seq_len), is P + num_seqs * max_splits * Hkv * 16 + 16 bytes, where
+ *    P = num_seqs * Hq * max_splits * (d + 2) * 4 rounded up to a multiple
+ *    of 16 (P = 0 when max_splits is 1).  pa_workspace_size(shape, num_seqs,
+ *    max_seq_len) is an upper bound of that need (it assumes the shortest
+ *    split), so a batch with pa_workspace_size <= PA_NOALLOC_SCRATCH_BYTES is
+ *    always accepted, and larger ones often are.
  *  - All calls share the one buffer and nothing in it needs clearing (every
  *    partial is written before it is read); calls whose kernels overlap on
  *    the GPU (different streams, no ordering) race on it.

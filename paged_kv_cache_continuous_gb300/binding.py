@@ -27,11 +27,10 @@ ERR_TIMEOUT = 7
 
 # Every symbol the two headers declare (checked by the tests).
 EXPORTS = [
-    "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode",
-    "pa_decode_noalloc", "pa_prefill",
-    "pa_mixed_step", "pa_copy_blocks", "pa_rope_append", "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_validation", "pa_check_device_error", "pa_last_error",
-    "pa_set_decode_split",
-    "pa_set_prefill_pairs",
+    "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode", "pa_decode_append",
+    "pa_decode_noalloc", "pa_prefill", "pa_mixed_step", "pa_copy_blocks", "pa_rope_append",
+    "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_validation", "pa_check_device_error", "pa_last_error",
+    "pa_set_decode_split", "pa_set_prefill_pairs",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
     "pa_alloc_num_free", "pa_alloc_num_blocks_of", "pa_alloc_block_table",
     "pa_sched_create", "pa_sched_destroy", "pa_sched_submit", "pa_sched_cancel", "pa_sched_plan",
@@ -84,6 +83,7 @@ def load():
         "pa_kv_append": ([SP, P, P, P, I, P, P, P], I),
         "pa_decode": ([SP, P, P, P, P, I, P, I, I, P, P, S, P], I),
         "pa_decode_noalloc": ([SP, P, P, P, P, I, P, I, I, P, P], I),
+        "pa_decode_append": ([SP, P, P, P, P, P, P, P, I, P, I, I, P, P, S, P], I),
         "pa_prefill": ([SP, P, P, P, P, P, P, I, I, I, I, P, P], I),
         "pa_mixed_step": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P], I),
         "pa_copy_blocks": ([SP, P, P, I, P, P, I, P, P, I, P], I),
@@ -265,6 +265,24 @@ def decode(shape, q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, ou
                             _bf16(v_pool, "v_pool"), _i32(block_table, "block_table"),
                             int(block_table.shape[1]), _i32(seq_lens, "seq_lens"), S, int(max_seq_len),
                             _bf16(out, "out"), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def decode_append(shape, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_table, seq_lens, max_seq_len: int,
+                  out=None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_decode_append: each sequence's new row appended at its slot, then
+    decode, in one launch (plus the merge)."""
+    S = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(shape, S, max_seq_len, q.device)
+    _check(load().pa_decode_append(ctypes.byref(_shape(shape)), _bf16(q, "q"), _bf16(k_new, "k_new"),
+                                   _bf16(v_new, "v_new"), _i32(slot_mapping, "slot_mapping"),
+                                   _bf16(k_pool, "k_pool"), _bf16(v_pool, "v_pool"),
+                                   _i32(block_table, "block_table"), int(block_table.shape[1]),
+                                   _i32(seq_lens, "seq_lens"), S, int(max_seq_len), _bf16(out, "out"), _ptr(ws),
+                                   ws.numel(), _stream(stream)))
     return out
 
 

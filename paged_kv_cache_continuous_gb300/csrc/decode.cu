@@ -8,14 +8,26 @@
 // with keys/values read through the block table from the KV head h / G.
 //
 // Design (GB300, HBM-bound):
-//  * One CTA per (split c, KV head g, sequence s).  A split covers
-//    `split_tokens` consecutive tokens, i.e. whole KV blocks.
-//  * A producer warp streams the split's blocks into an 8 (B=16) or
-//    4 (B=32) stage shared-memory ring with TMA tensor loads (128-byte
-//    swizzle), one mbarrier pair per stage.  Each block of one KV head is one
-//    contiguous B x d bf16 chunk of the pool, so a stage is 2 (K, V) x d/64
-//    boxes of B rows x 128 bytes.  Block ids are range-checked before use.
-//  * Four consumer warps take the stages round-robin.  Each warp computes the
+//  * Plan (decode_plan_kernel, the first step of the path): its first CTA
+//    lists the work items in the workspace -- one per (sequence, KV head,
+//    split of `split_tokens` consecutive tokens, i.e. whole KV blocks) that
+//    holds tokens: every full split first, then the last splits from longest
+//    to shortest.  Nothing is launched for splits a sequence does not have,
+//    so a ragged batch of short and long sequences costs what its tokens
+//    cost.  With the append fused (pa_decode_append, the mixed step), the
+//    launch's other CTAs copy the step's new rows into their slots.
+//  * Decode (decode_splitk_kernel, persistent, two CTAs per SM): CTA b
+//    takes items b, 2n-1-b, 2n+b, ... of the list (n CTAs; a snake order, so
+//    that the sorted sizes even out) and streams all of their KV blocks, one
+//    after another, through a ring of shared-memory stages filled by TMA
+//    tensor loads (128-byte swizzle): a producer warp whose lane l owns
+//    stage l walks the CTA's item sequence on its own and refills its stage
+//    as soon as it is free, with the next item's blocks while the current
+//    item is still being computed; another lane loads each item's G query
+//    rows into a q buffer as soon as the previous item's have been read.  Each block of one KV head is one contiguous B x d chunk of the
+//    pool, a stage is 2 (K, V) x d/64 boxes of B rows x 128 bytes.  Block ids
+//    are range-checked before use.
+//  * Four consumer warps take the blocks round-robin.  Each warp computes the
 //    scores of the G query heads of this KV head against 16 keys with
 //    m16n8k16 tensor-core MMAs (rows = query heads, padded to 16; the G
 //    heads share every K/V byte read), keeps its own online-softmax state
@@ -23,10 +35,14 @@
 //    tensor-core dot products keep the FP32 pipe free: with G = 8 a CUDA-core
 //    dot product would need ~2 G d FMAs per key, as much FP32 issue as the
 //    HBM stream leaves room for.
-//  * The warps' states are merged through shared memory; a sequence with a
-//    single split writes bf16 output directly, otherwise the (max, sum, acc)
-//    partials go to the workspace and decode_merge_kernel combines them.
+//  * At the end of an item the four states are merged in two steps through a
+//    small scratch area (warps 1 and 3 into 0 and 2, then 2 into 0; only the
+//    G rows that hold query heads) while the ring keeps filling; a sequence with a single split writes bf16 output
+//    directly, otherwise the (max, sum, acc) partials go to the workspace and
+//    decode_merge_kernel combines them.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -37,10 +53,9 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kQLane = 31;  // the producer lane that loads the items' query rows
 
-// FP8: the pools hold e4m3 codes (one byte per element) with one scale per KV
-// head for K and for V.
-template <int D, int BS, bool FP8 = false>
+template <int D, int BS, bool FP8, bool BIG_G>
 struct DecodeCfg {
     static constexpr int kEB = FP8 ? 1 : 2;                // bytes per pool element
     static constexpr int kBoxCols = 128 / kEB;             // elements per 128-byte TMA box row
@@ -48,366 +63,600 @@ struct DecodeCfg {
     static constexpr int kHalfBytes = BS * 128;            // one box: BS rows x 128 B
     static constexpr int kKVBytes = kHalves * kHalfBytes;  // K (or V) of one block
     static constexpr int kStageBytes = 2 * kKVBytes;
-    // multiple of kConsumerWarps; fp8 stages are half the bytes, so twice as
-    // many keep the same bytes in flight
-    static constexpr int kStages = ((BS == 16) ? 8 : 4) * (FP8 ? 2 : 1);
+    // 64 KB of blocks in flight per CTA.  A multiple of the consumer warps:
+    // stage st is read only by warp st % 4, block after block, so a warp
+    // never waits on a stage's barrier more than one phase ahead.
+    static constexpr int kStages = (65536 / kStageBytes) / kConsumerWarps * kConsumerWarps;
     static constexpr int kKSteps = D / 16;                 // QK^T k-steps
     static constexpr int kNTiles = D / 8;                  // PV n-tiles
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kScratchBytes = kConsumerWarps * 16 * D * 4 + kConsumerWarps * 16 * 8;
-    static constexpr int kRegionBytes = kRingBytes > kScratchBytes ? kRingBytes : kScratchBytes;
-    static constexpr int kSmemBytes = kRegionBytes + 2 * kStages * 8 + 16 + 1024;
+    // merge scratch: two slots of one warp's state (its MMA rows: 8, or 16
+    // for G > 8), rows padded by 8 floats
+    static constexpr int kRows = BIG_G ? 16 : 8;
+    static constexpr int kRow = D + 8;
+    static constexpr int kSlotFloats = kRows * kRow + kRows * 2;
+    static constexpr int kScratchOff = kRingBytes;
+    static constexpr int kQOff = kScratchOff + ((2 * kSlotFloats * 4 + 1023) / 1024) * 1024;
+    static constexpr int kQHalves = D / 64;                // q is bf16: 64-column boxes of G rows
+    static constexpr int kBarOff = kQOff + kQHalves * 2048;
+    static constexpr int kSmemBytes = kBarOff + (2 * kStages + 2) * 8 + 16 + 1024;
+    // two: a third would need the registers cut to 128 (spills; measured slower)
+    static constexpr int kCtasPerSm = 232448 / (kSmemBytes + 1024) < 2 ? 232448 / (kSmemBytes + 1024) : 2;
+    static_assert(kStages >= kConsumerWarps && kStages < kQLane, "one producer lane per stage, and the q lane");
 };
 
-__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
-    return *reinterpret_cast<const uint32_t *>(p);
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ bool len_ok(const DecodeArgs &a, int L, int BS) {
+    return L >= 0 && L <= a.max_seq_len && (L + BS - 1) / BS <= a.max_blocks;
+}
+
+// Exclusive prefix sum over the 1024 threads of the CTA; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int *tmp, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = tmp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        tmp[32 + lane] = t;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = warp ? tmp[32 + warp - 1] : 0;
+    *total = tmp[32 + 31];
+    __syncthreads();
+    return before + x - v;
+}
+
+constexpr int kPlanBins = 256;  // last-split sizes (in blocks) sorted by a counting sort
+
+// The plan launch.  CTA 0 (1024 threads, thread t owns a contiguous range of
+// sequences): a sequence of L > 0 tokens has ns = ceil(L / split) splits;
+// items (s, g, c, L) go first for every sequence's ns - 1 full splits, then
+// for the last splits, longest first (counting sort on their length in
+// blocks; equal lengths in no fixed order -- each item writes its own
+// outputs, so the order changes no result).  Empty sequences get zero
+// output here; a bad length sets the error word and gets no item.
+// CTAs 1.. (only with the append fused): row s of k_new / v_new, every KV
+// head, to slot_mapping[s] of the pools (16-byte pieces, grid-stride).
+template <int D, int BS>
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
+    __shared__ int tmp[64];
+    __shared__ int bins[kPlanBins];
+    // The decode kernel (launched as this one's programmatic dependent) may
+    // start now: it waits for this grid's completion before it reads
+    // anything this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (a.check_err_first && *(volatile int *)a.err != 0) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) a.plan_count[0] = 0;
+        return;
+    }
+    const int S = a.num_seqs, split = a.split_tokens, Hkv = a.num_kv_heads;
+    if (blockIdx.x > 0) {
+        constexpr int NV = D / 8;  // 16-byte pieces per row
+        const long long total = (long long)S * Hkv * NV;
+        for (long long x = (long long)(blockIdx.x - 1) * 1024 + threadIdx.x; x < total;
+             x += (long long)(gridDim.x - 1) * 1024) {
+            const int j = (int)(x % NV);
+            const long long sg = x / NV;
+            const int g = (int)(sg % Hkv), s = (int)(sg / Hkv);
+            const int slot = __ldg(a.slot_mapping + s);
+            if (slot < 0) continue;
+            if ((long long)slot >= a.num_slots) {
+                set_error(a.err, PA_ERR_BAD_INDEX);
+                continue;
+            }
+            const size_t dst = (((size_t)(slot / BS) * Hkv + g) * BS + slot % BS) * D;
+            const uint4 kx = __ldg(reinterpret_cast<const uint4 *>(a.k_new + sg * D) + j);
+            const uint4 vx = __ldg(reinterpret_cast<const uint4 *>(a.v_new + sg * D) + j);
+            reinterpret_cast<uint4 *>(a.k_pool + dst)[j] = kx;
+            reinterpret_cast<uint4 *>(a.v_pool + dst)[j] = vx;
+        }
+        return;
+    }
+    const int nbins = min(kPlanBins, (split + BS - 1) / BS);
+    // key 0 = the longest last split (nbins blocks or more)
+    auto key_of = [&](int L, int ns) { return nbins - min(nbins, (L - (ns - 1) * split + BS - 1) / BS); };
+    if (threadIdx.x < kPlanBins) bins[threadIdx.x] = 0;
+    __syncthreads();
+    const int per = (S + 1023) / 1024;
+    const int s_beg = min(S, (int)threadIdx.x * per), s_end = min(S, s_beg + per);
+    int nfull = 0;
+    for (int s = s_beg; s < s_end; ++s) {
+        const int L = a.seq_lens[s];
+        if (!len_ok(a, L, BS) || L == 0) continue;
+        const int ns = (L + split - 1) / split;
+        nfull += ns - 1;
+        atomicAdd(&bins[key_of(L, ns)], 1);
+    }
+    int total_full, total_last;
+    int pf = block_excl_scan(nfull, tmp, &total_full);
+    const int start = block_excl_scan(threadIdx.x < kPlanBins ? bins[threadIdx.x] : 0, tmp, &total_last);
+    if (threadIdx.x < kPlanBins) bins[threadIdx.x] = start;  // now the next free position of each size
+    __syncthreads();
+    for (int s = s_beg; s < s_end; ++s) {
+        const int L = a.seq_lens[s];
+        const bool ok = len_ok(a, L, BS);
+        if (!ok || L == 0) {
+            if (!ok) set_error(a.err, PA_ERR_BAD_INDEX);
+            if (ok) {  // an empty context attends to nothing: zeros
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * D);
+                for (int i = 0; i < a.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            continue;
+        }
+        const int ns = (L + split - 1) / split;
+        for (int c = 0; c < ns - 1; ++c)
+            for (int g = 0; g < Hkv; ++g) a.plan_items[(size_t)(pf + c) * Hkv + g] = make_int4(s, g, c, L);
+        pf += ns - 1;
+        const int pos = atomicAdd(&bins[key_of(L, ns)], 1);
+        for (int g = 0; g < Hkv; ++g)
+            a.plan_items[(size_t)(total_full + pos) * Hkv + g] = make_int4(s, g, ns - 1, L);
+    }
+    if (threadIdx.x == 0) a.plan_count[0] = (total_full + total_last) * Hkv;
+}
+
+// One work item as a warp holds it.
+struct Item {
+    int s, g, c, L, nsplit, t0, t1, nblk;
+    bool valid;
+};
+
+template <int BS>
+__device__ __forceinline__ Item load_item(const DecodeArgs &a, int k, int num_items) {
+    Item it;
+    it.valid = k < num_items;
+    const int4 v = it.valid ? a.plan_items[k] : make_int4(0, 0, 0, 0);
+    it.s = v.x;
+    it.g = v.y;
+    it.c = v.z;
+    it.L = v.w;
+    it.nsplit = it.valid ? (it.L + a.split_tokens - 1) / a.split_tokens : 1;
+    it.t0 = it.c * a.split_tokens;
+    it.t1 = min(it.L, it.t0 + a.split_tokens);
+    it.nblk = it.valid ? (it.t1 - it.t0 + BS - 1) / BS : 0;  // t0 is block aligned
+    return it;
 }
 
 template <int D, int BS, bool BIG_G, bool FP8>
-__global__ void __launch_bounds__(kThreads, 3)
-    decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasPerSm)
+    decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-    using C = DecodeCfg<D, BS, FP8>;
+    using C = DecodeCfg<D, BS, FP8, BIG_G>;
+    constexpr int kS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kRegionBytes);
-    uint64_t *empty = full + C::kStages;
-    int *s_abort = reinterpret_cast<int *>(empty + C::kStages);
-
-    const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    float *scratch = reinterpret_cast<float *>(smem + C::kScratchOff);
+    uint8_t *qbuf = smem + C::kQOff;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *empty = full + kS;
+    uint64_t *q_full = empty + kS;
+    uint64_t *q_empty = q_full + 1;
+    int *s_abort = reinterpret_cast<int *>(q_empty + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (a.check_err_first && *(volatile int *)a.err != 0) return;
-    const int L = a.seq_lens[s];
-    if (L < 0 || L > a.max_seq_len || (L + BS - 1) / BS > a.max_blocks) {
-        if (c == 0 && threadIdx.x == 0) set_error(a.err, PA_ERR_BAD_INDEX);
-        return;
-    }
-    const int nsplit = L > 0 ? (L + a.split_tokens - 1) / a.split_tokens : 1;
-    if (c >= nsplit) return;
-    const int t0 = c * a.split_tokens;
-    const int t1 = min(L, t0 + a.split_tokens);
-    const int nblk = (t1 - t0 + BS - 1) / BS;  // t0 is block aligned
-    const int b0 = t0 / BS;
-
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kStages; ++i) {
+        for (int i = 0; i < kS; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        *s_abort = 0;
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, kConsumerWarps);
+        // validation mode: skip everything if an earlier pass found a bad
+        // index (read once, so that the whole CTA takes the same branch)
+        *s_abort = (a.check_err_first && *(volatile int *)a.err != 0) ? 1 : 0;
         fence_barrier_init();
     }
     __syncthreads();
+    // Everything below reads what the plan launch wrote (the items, the
+    // appended rows): wait for it to complete.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (*(volatile int *)s_abort) return;
 
-    // ------------------------------------------------------------ producer --
+    const int num_items = a.plan_count[0];
+    const int nctas = gridDim.x;
+    auto item_at = [&](int j) {  // the CTA's j-th item (snake order over the list)
+        const int k = j * nctas + ((j & 1) ? nctas - 1 - (int)blockIdx.x : (int)blockIdx.x);
+        return load_item<BS>(a, k, num_items);
+    };
+
+    // ---------------------------------------------------------- producer --
     if (warp == kConsumerWarps) {
-        const int32_t *bt = a.block_table + (size_t)s * a.max_blocks + b0;
+        if (lane == kQLane) {
+            // The items' G query rows, item after item, into the one q buffer,
+            // each once the consumers have read the previous item's.
+            const uint32_t qbytes = (uint32_t)a.group * 128u * C::kQHalves;
+            tma_prefetch_desc(&tm_q);
+            int j = 0;
+            for (;; ++j) {
+                const Item it = item_at(j);
+                if (!it.valid) break;
+                if (j >= 1 && !mbar_wait(q_empty, (j - 1) & 1, a.err)) {
+                    atomicExch(s_abort, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full, qbytes);
+                const int qrow = it.s * a.num_q_heads + it.g * a.group;
+#pragma unroll
+                for (int hf = 0; hf < C::kQHalves; ++hf) tma_load_2d(qbuf + hf * 2048, &tm_q, q_full, hf * 64, qrow);
+            }
+            // after a timed-out wait: wait (bounded) for the last load in flight
+            if (j >= 1 && *(volatile int *)s_abort) mbar_wait(q_full, (j - 1) & 1, nullptr);
+            return;
+        }
+        if (lane >= kS) return;
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
-        // One lane per stage: lane l fills stage l with blocks l, l + kStages,
-        // ..., each as soon as the consumers have freed it, independently of
-        // the other lanes, so the TMA issue of a block overlaps its neighbours'.
-        constexpr int kLanes = C::kStages;
-        static_assert(kLanes <= 32, "one producer lane per stage");
-        int last = -1;  // the last block this lane issued (into stage `lane`)
-        bool good = true;
-        if (lane < kLanes) {
-            for (int i = lane; i < nblk; i += kLanes) {
-                int32_t blk = bt[i];
-                if ((unsigned)blk >= (unsigned)a.num_blocks) {
-                    set_error(a.err, PA_ERR_BAD_INDEX);
-                    blk = 0;  // never dereference an out-of-range block
-                }
-                if (i >= C::kStages && !mbar_wait(&empty[lane], ((i / C::kStages) - 1) & 1, a.err)) {
-                    good = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&full[lane], C::kStageBytes);
-                last = i;
-                uint8_t *sk = smem + lane * C::kStageBytes;
-                uint8_t *sv = sk + C::kKVBytes;
-                const int row = (blk * a.num_kv_heads + g) * BS;
+        // Lane l fills stage l with the CTA's blocks l, l + kS, l + 2 kS, ...
+        // (numbered across its items), each as soon as the consumer warp of
+        // the stage has freed it, independently of the other lanes.
+        int j = 0, base = 0;  // the item holding block gi, and its first block
+        Item it = item_at(0);
+        int last = -1;
+        for (int gi = lane;; gi += kS) {
+            while (it.valid && gi >= base + it.nblk) {
+                base += it.nblk;
+                it = item_at(++j);
+            }
+            if (!it.valid) break;
+            const int i = gi - base;
+            int32_t blk = a.block_table[(size_t)it.s * a.max_blocks + it.t0 / BS + i];
+            if ((unsigned)blk >= (unsigned)a.num_blocks) {
+                set_error(a.err, PA_ERR_BAD_INDEX);
+                blk = 0;  // never dereference an out-of-range block
+            }
+            if (gi >= kS && !mbar_wait(&empty[lane], ((gi / kS) - 1) & 1, a.err)) {
+                atomicExch(s_abort, 1);
+                break;
+            }
+            mbar_arrive_expect_tx(&full[lane], C::kStageBytes);
+            last = gi;
+            uint8_t *sk = smem + lane * C::kStageBytes;
+            uint8_t *sv = sk + C::kKVBytes;
+            const int row = (blk * a.num_kv_heads + it.g) * BS;
 #pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                    tma_load_2d(sk + hf * C::kHalfBytes, &tm_k, &full[lane], hf * C::kBoxCols, row);
-                    tma_load_2d(sv + hf * C::kHalfBytes, &tm_v, &full[lane], hf * C::kBoxCols, row);
-                }
+            for (int hf = 0; hf < C::kHalves; ++hf) {
+                tma_load_2d(sk + hf * C::kHalfBytes, &tm_k, &full[lane], hf * C::kBoxCols, row);
+                tma_load_2d(sv + hf * C::kHalfBytes, &tm_v, &full[lane], hf * C::kBoxCols, row);
             }
         }
-        if (!__all_sync(0xffffffffu, good) && lane == 0) atomicExch(s_abort, 1);
-        // Drain: every copy this CTA issued has landed before it may exit (a
-        // stage's earlier blocks were consumed before it was refilled).
-        if (last >= 0) mbar_wait(&full[lane], (last / C::kStages) & 1, a.err);
+        // Every block issued is consumed before the consumers leave, unless a
+        // wait timed out: then wait (bounded, not giving up on the error word)
+        // for this lane's copy in flight before leaving.
+        if (last >= 0 && *(volatile int *)s_abort) mbar_wait(&full[lane], (last / kS) & 1, nullptr);
         return;
     }
 
-    // ----------------------------------------------------------- consumers --
+    // --------------------------------------------------------- consumers --
     const int G = a.group;
-    const int r0 = lane >> 2;         // MMA row (query head within the group)
-    const int cq = (lane & 3) * 2;    // first of the lane's two columns
-    const __nv_bfloat16 *qg = a.q + ((size_t)s * a.num_q_heads + (size_t)g * G) * D;
-
-    uint32_t qa[C::kKSteps][4];
-    if (FP8) {
-        // fp16 A fragments with the k-step's 16 columns permuted to match the
-        // byte order ldmatrix gives the fp8 keys: MMA columns 2c, 2c+1 hold
-        // d = 4c, 4c+1 and columns 2c+8, 2c+9 hold d = 4c+2, 4c+3 (c = lane % 4).
-        const int c4 = (lane & 3) * 4;
-        auto qf = [&](int row, int col) {
-            return row < G ? pack_f16x2(__bfloat162float(qg[row * D + col]), __bfloat162float(qg[row * D + col + 1]))
+    const int r0 = lane >> 2;       // MMA row (query head within the group)
+    const int cq = (lane & 3) * 2;  // first of the lane's two columns
+    const uint32_t qb = smem_u32(qbuf);
+    int base = 0;                   // the CTA-wide index of the item's first block
+    bool ok = true;
+    for (int j = 0;; ++j) {
+        const Item it = item_at(j);
+        if (!it.valid) break;
+        const int s = it.s, g = it.g, t0 = it.t0, t1 = it.t1, nblk = it.nblk;
+        // ---- the item's query rows (row r of 64-column box hf at 2048 hf + 128 r, 128-byte swizzle)
+        if (!mbar_wait(q_full, j & 1, a.err)) ok = false;
+        uint32_t qa[C::kKSteps][4];
+        auto q2 = [&](int row, int col) {  // bf16 pair (col, col + 1) of a row
+            return row < G ? lds_u32(qb + (col >> 6) * 2048 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                                     (col & 7) * 2)
                            : 0u;
         };
+        if (FP8) {
+            // fp16 A fragments with the k-step's 16 columns permuted to match the
+            // byte order ldmatrix gives the fp8 keys: MMA columns 2c, 2c+1 hold
+            // d = 4c, 4c+1 and columns 2c+8, 2c+9 hold d = 4c+2, 4c+3 (c = lane % 4).
+            const int c4 = (lane & 3) * 4;
+            auto cvt = [](uint32_t v) {
+                const float2 f = bf16x2_unpack(v);
+                return pack_f16x2(f.x, f.y);
+            };
 #pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-            qa[ks][0] = qf(r0, ks * 16 + c4);
-            qa[ks][2] = qf(r0, ks * 16 + c4 + 2);
-            qa[ks][1] = BIG_G ? qf(r0 + 8, ks * 16 + c4) : 0u;
-            qa[ks][3] = BIG_G ? qf(r0 + 8, ks * 16 + c4 + 2) : 0u;
-        }
-    } else
-#pragma unroll
-    for (int ks = 0; ks < C::kKSteps; ++ks) {
-        qa[ks][0] = r0 < G ? ld_u32(qg + r0 * D + ks * 16 + cq) : 0u;
-        qa[ks][2] = r0 < G ? ld_u32(qg + r0 * D + ks * 16 + 8 + cq) : 0u;
-        if (BIG_G) {
-            qa[ks][1] = r0 + 8 < G ? ld_u32(qg + (r0 + 8) * D + ks * 16 + cq) : 0u;
-            qa[ks][3] = r0 + 8 < G ? ld_u32(qg + (r0 + 8) * D + ks * 16 + 8 + cq) : 0u;
+            for (int ks = 0; ks < C::kKSteps; ++ks) {
+                qa[ks][0] = cvt(q2(r0, ks * 16 + c4));
+                qa[ks][2] = cvt(q2(r0, ks * 16 + c4 + 2));
+                qa[ks][1] = BIG_G ? cvt(q2(r0 + 8, ks * 16 + c4)) : 0u;
+                qa[ks][3] = BIG_G ? cvt(q2(r0 + 8, ks * 16 + c4 + 2)) : 0u;
+            }
         } else {
-            qa[ks][1] = 0u;
-            qa[ks][3] = 0u;
+#pragma unroll
+            for (int ks = 0; ks < C::kKSteps; ++ks) {
+                qa[ks][0] = q2(r0, ks * 16 + cq);
+                qa[ks][2] = q2(r0, ks * 16 + 8 + cq);
+                qa[ks][1] = BIG_G ? q2(r0 + 8, ks * 16 + cq) : 0u;
+                qa[ks][3] = BIG_G ? q2(r0 + 8, ks * 16 + 8 + cq) : 0u;
+            }
         }
-    }
+        fence_proxy_async_smem();  // the next item's q load (async proxy) overwrites the buffer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_empty);
 
-    float acc[C::kNTiles][4];
+        float acc[C::kNTiles][4];
 #pragma unroll
-    for (int nt = 0; nt < C::kNTiles; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};  // rows r0, r0 + 8 (log2 units)
-    float l_run[2] = {0.f, 0.f};              // this lane's share of the row sums
-    const float sl = FP8 ? a.scale_log2 * a.k_scale[g] : a.scale_log2;
+        for (int nt = 0; nt < C::kNTiles; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY};  // rows r0, r0 + 8 (log2 units)
+        float l_run[2] = {0.f, 0.f};              // this lane's share of the row sums
+        const float sl = FP8 ? a.scale_log2 * a.k_scale[g] : a.scale_log2;
 
-    for (int i = warp; i < nblk; i += kConsumerWarps) {
-        const int st = i % C::kStages;
-        if (!mbar_wait(&full[st], (i / C::kStages) & 1, a.err)) {
-            atomicExch(s_abort, 1);
-            break;
-        }
-        const uint32_t sk = smem_u32(smem + st * C::kStageBytes);
-        const uint32_t sv = sk + C::kKVBytes;
-        const int tok0 = t0 + i * BS;
-        const int valid = t1 - tok0;  // tokens of this block that belong to the sequence
-        if (valid < BS) {
-            // Rows past the end of the sequence hold stale pool contents; P is
-            // zero there, but 0 * NaN would still poison the accumulator.
-            uint8_t *vz = smem + st * C::kStageBytes + C::kKVBytes;
-            for (int r = valid + (lane >> 3); r < BS; r += 4) {
-#pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf)
-                    *reinterpret_cast<uint4 *>(vz + hf * C::kHalfBytes + r * 128 + (lane & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+        // this warp's blocks: CTA-wide index = warp mod 4
+        for (int gi = base + (warp - base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+             ok && gi < base + nblk; gi += kConsumerWarps) {
+            const int i = gi - base;
+            const int st = gi % kS;
+            if (!mbar_wait(&full[st], (gi / kS) & 1, a.err)) {
+                ok = false;
+                break;
             }
-            __syncwarp();
-        }
+            const uint32_t sk = smem_u32(smem + st * C::kStageBytes);
+            const uint32_t sv = sk + C::kKVBytes;
+            const int tok0 = t0 + i * BS;
+            const int valid = t1 - tok0;  // tokens of this block that belong to the sequence
+            if (valid < BS) {
+                // Rows past the end of the sequence hold stale pool contents; P is
+                // zero there, but 0 * NaN would still poison the accumulator.
+                uint8_t *vz = smem + st * C::kStageBytes + C::kKVBytes;
+                for (int r = valid + (lane >> 3); r < BS; r += 4) {
 #pragma unroll
-        for (int sb = 0; sb < BS / 16; ++sb) {
-            if (sb * 16 >= valid) break;
-            // ---- S = Q K^T over 16 keys (two n-tiles of 8 keys)
-            float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            if (FP8) {
-                // one 16-byte chunk of a key row is one k-step; matrices: keys
-                // 0-7 / 8-15 x k-steps 2kp, 2kp+1.  A lane's 4 bytes are d = 4c..4c+3.
-                const int mat = lane >> 3;
-                const int t = sb * 16 + (lane & 7) + ((mat >> 1) << 3);
-#pragma unroll
-                for (int kp = 0; kp < C::kKSteps / 2; ++kp) {
-                    const int jj = 2 * kp + (mat & 1);
-                    const uint32_t addr = sk + t * 128 + (((jj ^ (t & 7))) << 4);
-                    uint32_t b00, b01, b10, b11;  // (keys 0-7, ks), (0-7, ks+1), (8-15, ks), (8-15, ks+1)
-                    ldmatrix_x4(addr, b00, b01, b10, b11);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int ks = 2 * kp + u;
-                        const uint32_t lo = u ? b01 : b00, hi = u ? b11 : b10;
-                        mma_f16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(lo),
-                                      e4m3x2_to_f16x2(lo >> 16));
-                        mma_f16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(hi),
-                                      e4m3x2_to_f16x2(hi >> 16));
-                    }
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        *reinterpret_cast<uint4 *>(vz + hf * C::kHalfBytes + r * 128 + (lane & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
                 }
-            } else {
-                const int mat = lane >> 3;
-                const int t = sb * 16 + (lane & 7) + ((mat >> 1) << 3);
-#pragma unroll
-                for (int ks = 0; ks < C::kKSteps; ++ks) {
-                    const int jj = 2 * ks + (mat & 1);  // 16-byte chunk over d
-                    const uint32_t addr = sk + (jj >> 3) * C::kHalfBytes + t * 128 +
-                                          ((((jj & 7) ^ (t & 7))) << 4);
-                    uint32_t b00, b01, b10, b11;
-                    ldmatrix_x4(addr, b00, b01, b10, b11);
-                    mma_bf16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-                    mma_bf16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
-                }
+                __syncwarp();
             }
-            // ---- online softmax (rows r0 and, for G > 8, r0 + 8)
-            const int nvalid = valid - sb * 16;  // keys of this sub-block in the sequence
-            float p[2][4];
-            float alpha[2] = {1.f, 1.f};
 #pragma unroll
-            for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
-                float x[4];
+            for (int sb = 0; sb < BS / 16; ++sb) {
+                if (sb * 16 >= valid) break;
+                // ---- S = Q K^T over 16 keys (two n-tiles of 8 keys)
+                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (FP8) {
+                    // one 16-byte chunk of a key row is one k-step; matrices: keys
+                    // 0-7 / 8-15 x k-steps 2kp, 2kp+1.  A lane's 4 bytes are d = 4c..4c+3.
+                    const int mat = lane >> 3;
+                    const int t = sb * 16 + (lane & 7) + ((mat >> 1) << 3);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                    for (int kp = 0; kp < C::kKSteps / 2; ++kp) {
+                        const int jj = 2 * kp + (mat & 1);
+                        const uint32_t addr = sk + t * 128 + (((jj ^ (t & 7))) << 4);
+                        uint32_t b00, b01, b10, b11;  // (keys 0-7, ks), (0-7, ks+1), (8-15, ks), (8-15, ks+1)
+                        ldmatrix_x4(addr, b00, b01, b10, b11);
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int key = nt * 8 + cq + e;
-                        x[nt * 2 + e] = key < nvalid ? sacc[nt][rr * 2 + e] * sl : -INFINITY;
-                    }
-                float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float mn = fmaxf(m_run[rr], mx);
-                alpha[rr] = fast_exp2(m_run[rr] - mn);
-                m_run[rr] = mn;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x[e] = fast_exp2(x[e] - mn);
-#pragma unroll
-                for (int nt = 0; nt < C::kNTiles; ++nt) {
-                    acc[nt][rr * 2 + 0] *= alpha[rr];
-                    acc[nt][rr * 2 + 1] *= alpha[rr];
-                }
-                p[0][rr * 2 + 0] = x[0];
-                p[0][rr * 2 + 1] = x[1];
-                p[1][rr * 2 + 0] = x[2];
-                p[1][rr * 2 + 1] = x[3];
-            }
-            if (!BIG_G) {
-                p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
-            }
-            auto pk = [&](float lo, float hi) { return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
-            auto psum = [&](uint32_t v) { return FP8 ? f16x2_sum(v) : bf16x2_sum(v); };
-            const uint32_t pa0 = pk(p[0][0], p[0][1]);
-            const uint32_t pa1 = pk(p[0][2], p[0][3]);
-            const uint32_t pa2 = pk(p[1][0], p[1][1]);
-            const uint32_t pa3 = pk(p[1][2], p[1][3]);
-            // The row sums use the same rounded weights that multiply V, so the
-            // output is an exact convex combination of the values.
-            l_run[0] = l_run[0] * alpha[0] + (psum(pa0) + psum(pa2));
-            if (BIG_G) l_run[1] = l_run[1] * alpha[1] + (psum(pa1) + psum(pa3));
-            // ---- acc += P V over the same 16 keys
-            if (FP8) {
-                // matrices: keys 0-7 / 8-15 x 16-byte d chunks 2jp, 2jp+1,
-                // transposed: a lane holds, per matrix, keys 2c, 2c+1 x d = 2n, 2n+1
-                // of the chunk (n = lane / 4).  Even d go to one n-tile, odd d
-                // to the next: acc[4 jp + 2 u + par] column 2c + e is
-                // d = 16 (2 jp + u) + 4c + 2e + par.
-                const int mat = lane >> 3;
-                const int t = sb * 16 + (lane & 7) + ((mat & 1) << 3);
-#pragma unroll
-                for (int jp = 0; jp < D / 32; ++jp) {
-                    const int jj = 2 * jp + (mat >> 1);
-                    const uint32_t addr = sv + t * 128 + (((jj ^ (t & 7))) << 4);
-                    uint32_t v0, v1, v2, v3;  // (keys 0-7, chunk 2jp), (8-15, 2jp), (0-7, 2jp+1), (8-15, 2jp+1)
-                    ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t lo = u ? v2 : v0, hi = u ? v3 : v1;
-#pragma unroll
-                        for (int par = 0; par < 2; ++par) {
-                            const uint32_t sel = par ? 0x3131u : 0x2020u;  // bytes (1, 3) or (0, 2)
-                            mma_f16_16816(acc[4 * jp + 2 * u + par], pa0, pa1, pa2, pa3,
-                                          e4m3x2_to_f16x2(__byte_perm(lo, 0u, sel)),
-                                          e4m3x2_to_f16x2(__byte_perm(hi, 0u, sel)));
+                        for (int u = 0; u < 2; ++u) {
+                            const int ks = 2 * kp + u;
+                            const uint32_t lo = u ? b01 : b00, hi = u ? b11 : b10;
+                            mma_f16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(lo),
+                                          e4m3x2_to_f16x2(lo >> 16));
+                            mma_f16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(hi),
+                                          e4m3x2_to_f16x2(hi >> 16));
                         }
                     }
+                } else {
+                    const int mat = lane >> 3;
+                    const int t = sb * 16 + (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+                    for (int ks = 0; ks < C::kKSteps; ++ks) {
+                        const int jj = 2 * ks + (mat & 1);  // 16-byte chunk over d
+                        const uint32_t addr = sk + (jj >> 3) * C::kHalfBytes + t * 128 +
+                                              ((((jj & 7) ^ (t & 7))) << 4);
+                        uint32_t b00, b01, b10, b11;
+                        ldmatrix_x4(addr, b00, b01, b10, b11);
+                        mma_bf16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
+                        mma_bf16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
+                    }
                 }
-            } else {
-                const int mat = lane >> 3;
-                const int t = sb * 16 + (lane & 7) + ((mat & 1) << 3);
+                // ---- online softmax (rows r0 and, for G > 8, r0 + 8)
+                const int nvalid = valid - sb * 16;  // keys of this sub-block in the sequence
+                float p[2][4];
+                float alpha[2] = {1.f, 1.f};
 #pragma unroll
-                for (int np = 0; np < C::kNTiles / 2; ++np) {
-                    const int jj = 2 * np + (mat >> 1);
-                    const uint32_t addr = sv + (jj >> 3) * C::kHalfBytes + t * 128 +
-                                          ((((jj & 7) ^ (t & 7))) << 4);
-                    uint32_t v0, v1, v2, v3;
-                    ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-                    mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
-                    mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
+                for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
+                    float x[4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = nt * 8 + cq + e;
+                            x[nt * 2 + e] = key < nvalid ? sacc[nt][rr * 2 + e] * sl : -INFINITY;
+                        }
+                    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float mn = fmaxf(m_run[rr], mx);
+                    alpha[rr] = fast_exp2(m_run[rr] - mn);
+                    m_run[rr] = mn;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) x[e] = fast_exp2(x[e] - mn);
+#pragma unroll
+                    for (int nt = 0; nt < C::kNTiles; ++nt) {
+                        acc[nt][rr * 2 + 0] *= alpha[rr];
+                        acc[nt][rr * 2 + 1] *= alpha[rr];
+                    }
+                    p[0][rr * 2 + 0] = x[0];
+                    p[0][rr * 2 + 1] = x[1];
+                    p[1][rr * 2 + 0] = x[2];
+                    p[1][rr * 2 + 1] = x[3];
+                }
+                if (!BIG_G) {
+                    p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
+                }
+                auto pk = [&](float lo, float hi) { return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
+                auto psum = [&](uint32_t v) { return FP8 ? f16x2_sum(v) : bf16x2_sum(v); };
+                const uint32_t pa0 = pk(p[0][0], p[0][1]);
+                const uint32_t pa1 = pk(p[0][2], p[0][3]);
+                const uint32_t pa2 = pk(p[1][0], p[1][1]);
+                const uint32_t pa3 = pk(p[1][2], p[1][3]);
+                // The row sums use the same rounded weights that multiply V, so the
+                // output is an exact convex combination of the values.
+                l_run[0] = l_run[0] * alpha[0] + (psum(pa0) + psum(pa2));
+                if (BIG_G) l_run[1] = l_run[1] * alpha[1] + (psum(pa1) + psum(pa3));
+                // ---- acc += P V over the same 16 keys
+                if (FP8) {
+                    // matrices: keys 0-7 / 8-15 x 16-byte d chunks 2jp, 2jp+1,
+                    // transposed: a lane holds, per matrix, keys 2c, 2c+1 x d = 2n, 2n+1
+                    // of the chunk (n = lane / 4).  Even d go to one n-tile, odd d
+                    // to the next: acc[4 jp + 2 u + par] column 2c + e is
+                    // d = 16 (2 jp + u) + 4c + 2e + par.
+                    const int mat = lane >> 3;
+                    const int t = sb * 16 + (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+                    for (int jp = 0; jp < D / 32; ++jp) {
+                        const int jj = 2 * jp + (mat >> 1);
+                        const uint32_t addr = sv + t * 128 + (((jj ^ (t & 7))) << 4);
+                        uint32_t v0, v1, v2, v3;  // (keys 0-7, chunk 2jp), (8-15, 2jp), (0-7, 2jp+1), (8-15, 2jp+1)
+                        ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const uint32_t lo = u ? v2 : v0, hi = u ? v3 : v1;
+#pragma unroll
+                            for (int par = 0; par < 2; ++par) {
+                                const uint32_t sel = par ? 0x3131u : 0x2020u;  // bytes (1, 3) or (0, 2)
+                                mma_f16_16816(acc[4 * jp + 2 * u + par], pa0, pa1, pa2, pa3,
+                                              e4m3x2_to_f16x2(__byte_perm(lo, 0u, sel)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, sel)));
+                            }
+                        }
+                    }
+                } else {
+                    const int mat = lane >> 3;
+                    const int t = sb * 16 + (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+                    for (int np = 0; np < C::kNTiles / 2; ++np) {
+                        const int jj = 2 * np + (mat >> 1);
+                        const uint32_t addr = sv + (jj >> 3) * C::kHalfBytes + t * 128 +
+                                              ((((jj & 7) ^ (t & 7))) << 4);
+                        uint32_t v0, v1, v2, v3;
+                        ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+                        mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
+                        mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        base += nblk;
+
+        // ------------------------------------------- merge the four states --
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
+            l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+        }
+        // element (row, column) of a lane's accumulator fragment
+        auto col_of = [&](int nt, int e) {
+            return FP8 ? 16 * (nt >> 1) + 4 * (lane & 3) + (nt & 1) + 2 * e : nt * 8 + cq + e;
+        };
+        auto put = [&](int slot) {  // this warp's state (its rows < G) into a scratch slot
+            float *sa = scratch + slot * C::kSlotFloats;
+#pragma unroll
+            for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
+                const int row = r0 + rr * 8;
+                if (row >= G) continue;
+#pragma unroll
+                for (int nt = 0; nt < C::kNTiles; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) sa[row * C::kRow + col_of(nt, e)] = acc[nt][rr * 2 + e];
+                if ((lane & 3) == 0) {
+                    sa[C::kRows * C::kRow + row * 2 + 0] = m_run[rr];
+                    sa[C::kRows * C::kRow + row * 2 + 1] = l_run[rr];
+                }
+            }
+        };
+        auto take = [&](int slot) {  // combine a scratch slot into this warp's state
+            const float *sa = scratch + slot * C::kSlotFloats;
+#pragma unroll
+            for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
+                const int row = r0 + rr * 8;
+                if (row >= G) continue;
+                const float mo = sa[C::kRows * C::kRow + row * 2 + 0], lo = sa[C::kRows * C::kRow + row * 2 + 1];
+                const float M = fmaxf(m_run[rr], mo);
+                const float fa = M == -INFINITY ? 0.f : fast_exp2(m_run[rr] - M);  // 0 for a warp that saw no key
+                const float fb = M == -INFINITY ? 0.f : fast_exp2(mo - M);
+#pragma unroll
+                for (int nt = 0; nt < C::kNTiles; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        acc[nt][rr * 2 + e] = acc[nt][rr * 2 + e] * fa + sa[row * C::kRow + col_of(nt, e)] * fb;
+                l_run[rr] = l_run[rr] * fa + lo * fb;
+                m_run[rr] = M;
+            }
+        };
+        auto csync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); };
+        // two steps: warps 1 and 3 into 0 and 2, then 2 into 0
+        csync();  // every warp is done with the item; the previous merge's reads are done
+        if (warp & 1) put(warp >> 1);
+        csync();
+        if (!(warp & 1)) take(warp >> 1);
+        csync();
+        if (warp == 2) put(0);
+        csync();
+        if (warp == 0) take(0);
+        if (warp == 0) {
+            const float vs = FP8 ? a.v_scale[g] : 1.f;
+#pragma unroll
+            for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
+                const int row = r0 + rr * 8;
+                if (row >= G) continue;
+                const int h = g * G + row;
+                if (it.nsplit == 1) {
+                    const float inv = l_run[rr] > 0.f ? vs / l_run[rr] : 0.f;
+                    __nv_bfloat16 *o = a.out + ((size_t)s * a.num_q_heads + h) * D;
+#pragma unroll
+                    for (int nt = 0; nt < C::kNTiles; ++nt) {
+                        if (FP8) {
+                            o[col_of(nt, 0)] = __float2bfloat16_rn(acc[nt][rr * 2 + 0] * inv);
+                            o[col_of(nt, 1)] = __float2bfloat16_rn(acc[nt][rr * 2 + 1] * inv);
+                        } else {
+                            *reinterpret_cast<__nv_bfloat162 *>(o + col_of(nt, 0)) =
+                                __floats2bfloat162_rn(acc[nt][rr * 2 + 0] * inv, acc[nt][rr * 2 + 1] * inv);
+                        }
+                    }
+                } else {
+                    const size_t pi = ((size_t)s * a.num_q_heads + h) * a.max_splits + it.c;
+                    float *pacc = a.part_acc + pi * D;
+#pragma unroll
+                    for (int nt = 0; nt < C::kNTiles; ++nt) {
+                        if (FP8) {
+                            pacc[col_of(nt, 0)] = acc[nt][rr * 2 + 0] * vs;
+                            pacc[col_of(nt, 1)] = acc[nt][rr * 2 + 1] * vs;
+                        } else {
+                            *reinterpret_cast<float2 *>(pacc + col_of(nt, 0)) =
+                                make_float2(acc[nt][rr * 2 + 0], acc[nt][rr * 2 + 1]);
+                        }
+                    }
+                    if ((lane & 3) == 0) {
+                        a.part_ml[pi * 2 + 0] = m_run[rr];
+                        a.part_ml[pi * 2 + 1] = l_run[rr];
+                    }
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-
-    // ----------------------------------------- merge the four warps' states --
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
-        l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
-    }
-    if (FP8) {
-        const float vs = a.v_scale[g];
-#pragma unroll
-        for (int nt = 0; nt < C::kNTiles; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] *= vs;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    float *red_acc = reinterpret_cast<float *>(smem);                       // [W][16][D]
-    float *red_ml = red_acc + kConsumerWarps * 16 * D;                      // [W][16][2]
-#pragma unroll
-    for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
-        const int row = r0 + rr * 8;
-        float *dst = red_acc + (warp * 16 + row) * D;
-#pragma unroll
-        for (int nt = 0; nt < C::kNTiles; ++nt) {
-            if (FP8) {
-                const int d0 = 16 * (nt >> 1) + 4 * (lane & 3) + (nt & 1);
-                dst[d0] = acc[nt][rr * 2 + 0];
-                dst[d0 + 2] = acc[nt][rr * 2 + 1];
-            } else {
-                *reinterpret_cast<float2 *>(dst + nt * 8 + cq) = make_float2(acc[nt][rr * 2 + 0], acc[nt][rr * 2 + 1]);
-            }
-        }
-        if ((lane & 3) == 0) {
-            red_ml[(warp * 16 + row) * 2 + 0] = m_run[rr];
-            red_ml[(warp * 16 + row) * 2 + 1] = l_run[rr];
-        }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    if (*(volatile int *)s_abort) return;
-
-    const int tid = threadIdx.x;  // 0 .. 127
-    for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
-        const int row = idx / D, e = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[(w * 16 + row) * 2]);
-        float sum_l = 0.f, sum_a = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = red_ml[(w * 16 + row) * 2];
-                const float f = fast_exp2(mw - M);  // 0 for a warp that saw no key
-                sum_l += f * red_ml[(w * 16 + row) * 2 + 1];
-                sum_a += f * red_acc[(w * 16 + row) * D + e];
-            }
-        }
-        const int h = g * G + row;
-        if (nsplit == 1) {
-            const float o = sum_l > 0.f ? sum_a / sum_l : 0.f;
-            a.out[((size_t)s * a.num_q_heads + h) * D + e] = __float2bfloat16_rn(o);
-        } else {
-            const size_t pi = ((size_t)s * a.num_q_heads + h) * a.max_splits + c;
-            a.part_acc[pi * D + e] = sum_a;
-            if (e == 0) {
-                a.part_ml[pi * 2 + 0] = M;
-                a.part_ml[pi * 2 + 1] = sum_l;
-            }
-        }
+        // every consumer warp takes the same number of barriers, and leaves
+        // together once a wait has failed
+        if (!ok) atomicExch(s_abort, 1);
+        csync();
+        if (*(volatile int *)s_abort) break;
     }
 }
 
@@ -415,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 // one split: out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode kernel's partials
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x * 4 + warp, s = blockIdx.y;
     if (h >= a.num_q_heads) return;
@@ -458,20 +708,46 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
 }
 
 template <int D, int BS, bool BIG_G, bool FP8>
-cudaError_t launch_decode_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                            cudaStream_t stream) {
-    using C = DecodeCfg<D, BS, FP8>;
+cudaError_t launch_decode_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                            const DecodeArgs &a, int num_sms, cudaStream_t stream) {
+    using C = DecodeCfg<D, BS, FP8, BIG_G>;
     static std::atomic<unsigned long long> opted{0};
-    cudaError_t e0 = opt_in_smem(reinterpret_cast<const void *>(decode_splitk_kernel<D, BS, BIG_G, FP8>),
-                                 C::kSmemBytes, opted);
-    if (e0 != cudaSuccess) return e0;
-    dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-    decode_splitk_kernel<D, BS, BIG_G, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_k, tm_v, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(decode_splitk_kernel<D, BS, BIG_G, FP8>),
+                                C::kSmemBytes, opted);
+    if (e != cudaSuccess) return e;
+    // the plan's CTA, plus CTAs for the fused append (up to one per SM)
+    int plan_ctas = 1;
+    if (a.k_new) {
+        const long long pieces = (long long)a.num_seqs * a.num_kv_heads * (D / 8);
+        plan_ctas += (int)std::min<long long>(std::max(num_sms, 1), (pieces + 1023) / 1024);
+    }
+    decode_plan_kernel<D, BS><<<plan_ctas, 1024, 0, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // Persistent: as many CTAs per SM as fit, fewer when the items (counted
+    // on the device; at most every split of every sequence) cannot fill them.
+    const long long bound = (long long)a.num_seqs * a.num_kv_heads * a.max_splits;
+    const long long ctas =
+        std::max(1LL, std::min<long long>((long long)C::kCtasPerSm * std::max(num_sms, 1), bound));
+    // Programmatic dependent launches: each kernel's CTAs are placed while
+    // the previous one still runs and wait for it in griddepcontrol.wait, so
+    // the launch gaps between the three kernels overlap the work.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_splitk_kernel<D, BS, BIG_G, FP8>, tm_q, tm_k, tm_v, a);
     if (e != cudaSuccess || a.max_splits <= 1) return e;
-    dim3 mgrid((a.num_q_heads + 3) / 4, a.num_seqs);
-    decode_merge_kernel<D><<<mgrid, 128, 0, stream>>>(a);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((a.num_q_heads + 3) / 4, a.num_seqs);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a);
 }
 
 }  // namespace
@@ -493,19 +769,35 @@ int decode_max_splits(int max_seq_len, int split_tokens) {
     return max_seq_len > 0 ? (max_seq_len + split_tokens - 1) / split_tokens : 1;
 }
 
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits) {
+// Layout: [part_acc S*Hq*max_splits*d floats][part_ml S*Hq*max_splits*2
+// floats] (only when max_splits > 1), then the plan, 16-byte aligned:
+// [items: S * max_splits * Hkv int4][count: 4 ints].
+static size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits) {
     if (max_splits <= 1) return 0;
     const size_t n = (size_t)num_seqs * num_q_heads * max_splits;
-    return n * head_dim * sizeof(float) + n * 2 * sizeof(float);
+    return (n * head_dim * sizeof(float) + n * 2 * sizeof(float) + 15) & ~size_t(15);
 }
 
-cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, int block_size, cudaStream_t stream, bool fp8) {
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits) {
+    return partials_bytes(num_seqs, num_q_heads, head_dim, max_splits) +
+           (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4) + 4 * sizeof(int);
+}
+
+void decode_plan_layout(void *ws, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits,
+                        int4 **items, int **count) {
+    uint8_t *p = static_cast<uint8_t *>(ws) + partials_bytes(num_seqs, num_q_heads, head_dim, max_splits);
+    *items = reinterpret_cast<int4 *>(p);
+    *count = reinterpret_cast<int *>(p + (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4));
+}
+
+cudaError_t launch_decode(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                          const DecodeArgs &a, int head_dim, int block_size, int num_sms, cudaStream_t stream,
+                          bool fp8) {
     const bool big = a.group > 8;
-#define PA_DEC(D, BS, F8)                                                              \
-    if (head_dim == D && block_size == BS && fp8 == F8)                                \
-        return big ? launch_decode_t<D, BS, true, F8>(tm_k, tm_v, a, stream)           \
-                   : launch_decode_t<D, BS, false, F8>(tm_k, tm_v, a, stream);
+#define PA_DEC(D, BS, F8)                                                                   \
+    if (head_dim == D && block_size == BS && fp8 == F8)                                     \
+        return big ? launch_decode_t<D, BS, true, F8>(tm_q, tm_k, tm_v, a, num_sms, stream) \
+                   : launch_decode_t<D, BS, false, F8>(tm_q, tm_k, tm_v, a, num_sms, stream);
     PA_DEC(128, 16, false)
     PA_DEC(128, 32, false)
     PA_DEC(64, 16, false)

@@ -8,6 +8,10 @@
 // slot < 0 is padding.  A pure bit copy: 16-byte vector loads and stores,
 // consecutive threads on consecutive 16-byte pieces of one (token, head) row,
 // so both the read of k_new and the write into the pool are coalesced.
+// (Decode steps can instead append their rows inside the decode kernel:
+// pa_decode_append.)
+#include <algorithm>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -15,30 +19,51 @@ namespace pa {
 
 namespace {
 
+// Each thread moves kAppendU 16-byte pieces of K and of V per pass of a
+// grid-stride loop; the loads of a pass (the pieces and their slots) are all
+// issued before any of them is used, and the pieces of one thread are a CTA
+// width apart, so every load and store instruction of a warp covers 512
+// contiguous bytes.  32-bit index arithmetic (the host checks that
+// T * Hkv * d / 8 fits).
+constexpr int kAppendU = 2;
+
+template <int VPR>  // 16-byte pieces per row: d / 8
 __global__ void __launch_bounds__(256)
     kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
-                     const int32_t *__restrict__ slot_mapping, long long num_vec, int vec_per_row,
-                     int num_kv_heads, int block_size, long long num_slots, uint4 *__restrict__ k_pool,
-                     uint4 *__restrict__ v_pool, int *err, int check_err_first) {
+                     const int32_t *__restrict__ slot_mapping, int num_vec, int num_kv_heads, int block_size,
+                     long long num_slots, uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int *err,
+                     int check_err_first) {
     if (check_err_first && *(volatile int *)err != 0) return;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < num_vec; idx += stride) {
-        const int j = (int)(idx % vec_per_row);             // 16-byte piece within the row
-        const long long th = idx / vec_per_row;             // token * Hkv + head
-        const int h = (int)(th % num_kv_heads);
-        const long long tok = th / num_kv_heads;
-        const int slot = __ldg(slot_mapping + tok);
-        if (slot < 0) continue;
-        if ((long long)slot >= num_slots) {
-            set_error(err, PA_ERR_BAD_INDEX);
-            continue;
+    const int step = gridDim.x * (256 * kAppendU);
+    for (int base = blockIdx.x * (256 * kAppendU) + threadIdx.x; base < num_vec; base += step) {
+        uint4 kv[kAppendU], vv[kAppendU];
+        int slot[kAppendU], th[kAppendU];
+#pragma unroll
+        for (int u = 0; u < kAppendU; ++u) {
+            const int idx = base + u * 256;
+            slot[u] = -1;
+            if (idx < num_vec) {
+                th[u] = idx / VPR;  // token * Hkv + head
+                slot[u] = __ldg(slot_mapping + th[u] / num_kv_heads);
+                kv[u] = __ldg(k_new + idx);
+                vv[u] = __ldg(v_new + idx);
+            }
         }
-        const long long blk = slot / block_size, off = slot % block_size;
-        const long long dst = ((blk * num_kv_heads + h) * block_size + off) * vec_per_row + j;
-        const uint4 kv = __ldg(k_new + idx);
-        const uint4 vv = __ldg(v_new + idx);
-        k_pool[dst] = kv;
-        v_pool[dst] = vv;
+#pragma unroll
+        for (int u = 0; u < kAppendU; ++u) {
+            const int sl = slot[u];
+            if (sl < 0) continue;
+            if ((long long)sl >= num_slots) {
+                set_error(err, PA_ERR_BAD_INDEX);
+                continue;
+            }
+            const int idx = base + u * 256;
+            const int tok = th[u] / num_kv_heads, h = th[u] - tok * num_kv_heads;
+            const int blk = sl / block_size, off = sl - blk * block_size;
+            const long long dst = (((long long)blk * num_kv_heads + h) * block_size + off) * VPR + (idx % VPR);
+            k_pool[dst] = kv[u];
+            v_pool[dst] = vv[u];
+        }
     }
 }
 
@@ -132,6 +157,17 @@ __global__ void __launch_bounds__(256) index_check_kernel(const CheckArgs a) {
                 const int blk = a.block_table[(size_t)s * a.max_blocks + b];
                 if (blk < 0 || blk >= a.num_blocks) set_error(a.err, PA_ERR_BAD_INDEX);
             }
+            // A fused append writes row s inside the decode of sequence s: its
+            // slot must be the sequence's last position (or padding).
+            if (a.decode_slots && a.slot_mapping && s < a.decode_rows) {
+                const int sl = a.slot_mapping[s];
+                const int p = L - 1;
+                if (sl >= 0 && (p < 0 || (long long)sl != (long long)a.block_table[(size_t)s * a.max_blocks +
+                                                                                    p / a.block_size] *
+                                                                                   a.block_size +
+                                                                               p % a.block_size))
+                    set_error(a.err, PA_ERR_BAD_INDEX);
+            }
         }
     }
 }
@@ -141,18 +177,26 @@ __global__ void __launch_bounds__(256) index_check_kernel(const CheckArgs a) {
 cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
                              const int32_t *slot_mapping, int num_tokens, int num_kv_heads,
                              int head_dim, int block_size, int num_blocks, __nv_bfloat16 *k_pool,
-                             __nv_bfloat16 *v_pool, int *err, int check_err_first,
+                             __nv_bfloat16 *v_pool, int *err, int check_err_first, int num_sms,
                              cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
-    const int vec_per_row = head_dim / 8;
-    const long long num_vec = (long long)num_tokens * num_kv_heads * vec_per_row;
-    const int threads = 256;
-    long long blocks = (num_vec + threads - 1) / threads;
-    if (blocks > 152LL * 16) blocks = 152LL * 16;  // grid-stride beyond 16 CTAs per SM
-    kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slot_mapping,
-        num_vec, vec_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size,
-        reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool), err, check_err_first);
+    const long long nv = (long long)num_tokens * num_kv_heads * (head_dim / 8);
+    if (nv > 0x7fffffffLL - 256LL * kAppendU) return cudaErrorInvalidValue;
+    const int num_vec = (int)nv;
+    // Up to 8 CTAs of 256 threads per SM; larger steps loop (grid stride).
+    const unsigned blocks = (unsigned)std::min<long long>((num_vec + 256 * kAppendU - 1) / (256 * kAppendU),
+                                                          8LL * std::max(num_sms, 1));
+    const long long slots = (long long)num_blocks * block_size;
+    auto *kp = reinterpret_cast<uint4 *>(k_pool);
+    auto *vp = reinterpret_cast<uint4 *>(v_pool);
+    auto *kn = reinterpret_cast<const uint4 *>(k_new);
+    auto *vn = reinterpret_cast<const uint4 *>(v_new);
+    if (head_dim == 128)
+        kv_append_kernel<16><<<blocks, 256, 0, stream>>>(kn, vn, slot_mapping, num_vec, num_kv_heads, block_size,
+                                                         slots, kp, vp, err, check_err_first);
+    else
+        kv_append_kernel<8><<<blocks, 256, 0, stream>>>(kn, vn, slot_mapping, num_vec, num_kv_heads, block_size,
+                                                        slots, kp, vp, err, check_err_first);
     return cudaGetLastError();
 }
 

@@ -179,6 +179,22 @@ int make_rows_map(CUtensorMap *m, const void *base, int head_dim, int heads, lon
     return PA_OK;
 }
 
+// q of a decode batch as rows [S * Hq][d] bf16; box = 64 columns x G rows
+// (the query heads of one KV head), 128-byte swizzle.
+int make_qgroup_map(CUtensorMap *m, const void *q, const pa_shape_t *sh, int num_seqs) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)sh->head_dim, (cuuint64_t)num_seqs * sh->num_q_heads};
+    const cuuint64_t strides[1] = {(cuuint64_t)sh->head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(sh->num_q_heads / sh->num_kv_heads)};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed");
+    return PA_OK;
+}
+
 int split_min_tokens(int block_size) {
     const int ov = g_split_override.load();
     const int base = ov > 0 ? ov : 256;
@@ -188,11 +204,13 @@ int split_min_tokens(int block_size) {
 // ---------------------------------------------------------- the three ops --
 int do_append(const pa_shape_t *sh, const void *k_new, const void *v_new, const int32_t *slots,
               int num_tokens, void *k_pool, void *v_pool, cudaStream_t st, DevState *d, int check_first) {
+    if ((long long)num_tokens * sh->num_kv_heads * (sh->head_dim / 8) > 0x7fffffffLL - 4096)
+        return fail(PA_ERR_UNSUPPORTED, "append: num_tokens * num_kv_heads * head_dim / 8 must be below 2^31");
     cudaError_t e = launch_kv_append(static_cast<const __nv_bfloat16 *>(k_new),
                                      static_cast<const __nv_bfloat16 *>(v_new), slots, num_tokens,
                                      sh->num_kv_heads, sh->head_dim, sh->block_size, sh->num_blocks,
                                      static_cast<__nv_bfloat16 *>(k_pool), static_cast<__nv_bfloat16 *>(v_pool),
-                                     d->err, check_first, st);
+                                     d->err, check_first, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
     return PA_OK;
 }
@@ -201,7 +219,8 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
               const int32_t *block_table, int max_blocks, const int32_t *seq_lens, int num_seqs,
               int max_seq_len, void *out, void *ws, size_t ws_bytes, cudaStream_t st, DevState *d,
               int check_first, const float *k_scale = nullptr, const float *v_scale = nullptr,
-              int split_planned = 0) {
+              int split_planned = 0, const void *k_new = nullptr, const void *v_new = nullptr,
+              const int32_t *slot_mapping = nullptr) {
     const bool fp8 = k_scale != nullptr;
     // split_planned > 0: the caller has already planned the split (and sized
     // its scratch from it); the override is not read a second time.
@@ -209,12 +228,18 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
                                         : decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len,
                                                               sh->block_size, d->num_sms, g_split_override.load());
     const int max_splits = decode_max_splits(max_seq_len, split);
-    const size_t need = decode_workspace_bytes(num_seqs, sh->num_q_heads, sh->head_dim, max_splits);
-    if (need > 0 && (ws == nullptr || ws_bytes < need))
+    const size_t need = decode_workspace_bytes(num_seqs, sh->num_q_heads, sh->num_kv_heads, sh->head_dim,
+                                               max_splits);
+    if (ws == nullptr || ws_bytes < need)
         return fail(PA_ERR_WORKSPACE, "workspace smaller than " + std::to_string(need) + " bytes");
-    if (need > 0 && !aligned16(ws)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    CUtensorMap tk, tv;
-    int rc = fp8 ? make_pool_map_u8(&tk, k_pool, sh) : make_pool_map(&tk, k_pool, sh);
+    if (!aligned16(ws)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    if ((long long)num_seqs * sh->num_q_heads > 0x7fffffffLL ||
+        (long long)num_seqs * sh->num_kv_heads * max_splits > 0x7fffffffLL)
+        return fail(PA_ERR_UNSUPPORTED, "decode batch too large");
+    CUtensorMap tq, tk, tv;
+    int rc = make_qgroup_map(&tq, q, sh, num_seqs);
+    if (rc) return rc;
+    rc = fp8 ? make_pool_map_u8(&tk, k_pool, sh) : make_pool_map(&tk, k_pool, sh);
     if (rc) return rc;
     rc = fp8 ? make_pool_map_u8(&tv, v_pool, sh) : make_pool_map(&tv, v_pool, sh);
     if (rc) return rc;
@@ -225,9 +250,12 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
     a.block_table = block_table;
     a.seq_lens = seq_lens;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    a.part_acc = static_cast<float *>(ws);
-    a.part_ml = need ? static_cast<float *>(ws) + (size_t)num_seqs * sh->num_q_heads * max_splits * sh->head_dim
-                     : nullptr;
+    a.part_acc = max_splits > 1 ? static_cast<float *>(ws) : nullptr;
+    a.part_ml = max_splits > 1
+                    ? static_cast<float *>(ws) + (size_t)num_seqs * sh->num_q_heads * max_splits * sh->head_dim
+                    : nullptr;
+    decode_plan_layout(ws, num_seqs, sh->num_q_heads, sh->num_kv_heads, sh->head_dim, max_splits, &a.plan_items,
+                       &a.plan_count);
     a.err = d->err;
     a.num_seqs = num_seqs;
     a.num_q_heads = sh->num_q_heads;
@@ -240,7 +268,15 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
     a.max_seq_len = max_seq_len;
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
-    cudaError_t e = launch_decode(tk, tv, a, sh->head_dim, sh->block_size, st, fp8);
+    if (k_new) {
+        a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+        a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+        a.slot_mapping = slot_mapping;
+        a.k_pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(k_pool));
+        a.v_pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_pool));
+        a.num_slots = (long long)sh->num_blocks * sh->block_size;
+    }
+    cudaError_t e = launch_decode(tq, tk, tv, a, sh->head_dim, sh->block_size, d->num_sms, st, fp8);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return PA_OK;
 }
@@ -327,7 +363,7 @@ int noalloc_scratch(void **out) {
 // callers' fork/join sequences from interleaving.
 struct SideStream {
     cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, appended = nullptr, join = nullptr;
 };
 std::mutex g_side_mu;
 SideStream g_side[64];
@@ -343,6 +379,7 @@ int side_stream(SideStream **out) {
         e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
         if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, hi);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.appended, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
         if (e != cudaSuccess) return cuda_fail(e, "creating the mixed-step side stream");
     }
@@ -368,7 +405,7 @@ int pa_workspace_size(const pa_shape_t *shape, int max_seqs, int max_seq_len, si
     if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is NULL");
     if (max_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
     const int split = split_min_tokens(shape->block_size);
-    *bytes = decode_workspace_bytes(max_seqs, shape->num_q_heads, shape->head_dim,
+    *bytes = decode_workspace_bytes(max_seqs, shape->num_q_heads, shape->num_kv_heads, shape->head_dim,
                                     decode_max_splits(max_seq_len, split));
     return ok();
 }
@@ -541,6 +578,50 @@ int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool, const 
     return ok();
 }
 
+int pa_decode_append(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                     const int32_t *slot_mapping, void *k_pool, void *v_pool, const int32_t *block_table,
+                     int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, void *out,
+                     void *workspace, size_t ws_bytes, void *stream) {
+    Range range_("pa_decode_append");
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_seqs == 0) return ok();
+    if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");
+    if (!q || !k_new || !v_new || !slot_mapping || !k_pool || !v_pool || !block_table || !seq_lens || !out)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+    if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+    if ((max_seq_len + shape->block_size - 1) / shape->block_size > max_blocks_per_seq)
+        return fail(PA_ERR_INVALID_ARG, "max_seq_len does not fit in max_blocks_per_seq blocks");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(out))
+        return fail(PA_ERR_INVALID_ARG, "q, k/v, pools and out must be 16-byte aligned");
+    DevState *d;
+    if ((rc = dev_state(&d))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int val = g_validation.load();
+    if (val) {
+        CheckArgs ca{};
+        ca.slot_mapping = slot_mapping;
+        ca.num_tokens = num_seqs;
+        ca.block_table = block_table;
+        ca.seq_lens = seq_lens;
+        ca.num_seqs = num_seqs;
+        ca.max_blocks = max_blocks_per_seq;
+        ca.block_size = shape->block_size;
+        ca.num_blocks = shape->num_blocks;
+        ca.max_seq_len = max_seq_len;
+        ca.decode_rows = num_seqs;
+        ca.decode_slots = 1;
+        ca.err = d->err;
+        if ((rc = run_check(ca, st))) return rc;
+    }
+    rc = do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                   out, workspace, ws_bytes, st, d, val, nullptr, nullptr, 0, k_new, v_new, slot_mapping);
+    if (rc) return rc;
+    return ok();
+}
+
 int pa_kv_append_fp8(const pa_shape_t *shape, const void *k_new, const void *v_new, const int32_t *slot_mapping,
                      int num_tokens, const float *k_scale, const float *v_scale, void *k_pool, void *v_pool,
                      void *stream) {
@@ -635,7 +716,7 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
     if ((rc = dev_state(&d))) return rc;
     const int split = decode_split_tokens(num_seqs, shape->num_kv_heads, max_seq_len, shape->block_size,
                                           d->num_sms, g_split_override.load());
-    const size_t need = decode_workspace_bytes(num_seqs, shape->num_q_heads, shape->head_dim,
+    const size_t need = decode_workspace_bytes(num_seqs, shape->num_q_heads, shape->num_kv_heads, shape->head_dim,
                                                decode_max_splits(max_seq_len, split));
     if (need > PA_NOALLOC_SCRATCH_BYTES)
         return fail(PA_ERR_WORKSPACE, "batch needs " + std::to_string(need) +
@@ -746,14 +827,23 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
         ca.max_seq_len = max_seq_len;
         ca.max_q_len = max_q_len > 1 ? max_q_len : 1;
         ca.decode_rows = num_decode;
+        ca.decode_slots = 1;
         ca.err = d->err;
         if ((rc = run_check(ca, st))) return rc;
     }
-    if (num_tokens > 0 &&
-        (rc = do_append(shape, k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, st, d, val)))
-        return rc;
+    // Decode rows [0, num_decode) are appended inside the decode kernel (each
+    // by the CTA that reads that sequence's last block); the prompt rows
+    // [num_decode, num_tokens) by the append kernel ahead of the prefill.
     const int np = num_seqs - num_decode;
     const bool has_prefill = np > 0 && max_q_len > 0 && num_tokens > 0;
+    const size_t row = (size_t)shape->num_kv_heads * shape->head_dim;
+    const int prompt_rows = num_tokens - num_decode;
+    auto append_prompts = [&](cudaStream_t s) {
+        if (prompt_rows <= 0) return (int)PA_OK;
+        return do_append(shape, static_cast<const __nv_bfloat16 *>(k_new) + (size_t)num_decode * row,
+                         static_cast<const __nv_bfloat16 *>(v_new) + (size_t)num_decode * row,
+                         slot_mapping + num_decode, prompt_rows, k_pool, v_pool, s, d, val);
+    };
     auto prefill_on = [&](cudaStream_t s) {
         return do_prefill(shape, q, k_pool, v_pool, q_start_loc + num_decode, nullptr, seq_lens + num_decode,
                           block_table + (size_t)num_decode * max_blocks_per_seq, max_blocks_per_seq, np,
@@ -761,7 +851,8 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
     };
     auto decode_on = [&](cudaStream_t s) {
         return do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_decode,
-                         max_seq_len, out, workspace, ws_bytes, s, d, val);
+                         max_seq_len, out, workspace, ws_bytes, s, d, val, nullptr, nullptr, 0, k_new, v_new,
+                         slot_mapping);
     };
     if (num_decode > 0 && has_prefill) {
         std::lock_guard<std::mutex> lk(g_side_mu);
@@ -770,7 +861,17 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
         cudaError_t e = cudaEventRecord(side->fork, st);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
         if (e != cudaSuccess) return cuda_fail(e, "forking the mixed step");
-        rc = prefill_on(side->stream);
+        // The decode waits for the prompt rows' append too: then the prefill
+        // (higher priority) and the decode become ready together, and the
+        // prefill's persistent CTA pairs -- one per SM, too large to share one
+        // with decode CTAs -- are placed first, on the SMs the decode then
+        // leaves to them.  (A decode started earlier would take every SM and
+        // the prefill would only start as it drains.)
+        rc = append_prompts(side->stream);
+        if (e == cudaSuccess) e = cudaEventRecord(side->appended, side->stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->appended, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "ordering the mixed step");
+        if (!rc) rc = prefill_on(side->stream);
         const int rc2 = decode_on(st);
         e = cudaEventRecord(side->join, side->stream);  // join even after a failed launch
         if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
@@ -780,6 +881,7 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
         return ok();
     }
     if (num_decode > 0 && (rc = decode_on(st))) return rc;
+    if ((rc = append_prompts(st))) return rc;
     if (has_prefill && (rc = prefill_on(st))) return rc;
     return ok();
 }

@@ -40,22 +40,42 @@ struct DecodeArgs {
     int check_err_first;         // validation mode: skip work if *err != 0
     float scale_log2;            // softmax scale * log2(e)
     const float *k_scale, *v_scale;  // fp8 pools: [Hkv] scales (value = code * scale); else null
+    // Fused append (pa_decode_append; null otherwise): row s of k_new / v_new
+    // [S][Hkv][d] goes to slot_mapping[s] of the pools before it is read.
+    const __nv_bfloat16 *k_new, *v_new;
+    const int32_t *slot_mapping;
+    __nv_bfloat16 *k_pool, *v_pool;
+    long long num_slots;
+    // The plan (first step of the path): decode_plan_kernel writes the work
+    // items -- (sequence, KV head, split, length) -- into the workspace and
+    // plan_count[0] = their number.
+    int4 *plan_items;
+    int *plan_count;
 };
 
 // Tokens per split-K chunk chosen for a decode batch (multiple of block_size).
 int decode_split_tokens(int num_seqs, int num_kv_heads, int max_seq_len, int block_size,
                         int num_sms, int override_tokens);
 int decode_max_splits(int max_seq_len, int split_tokens);
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits);
+// Workspace of one decode call: split partials (when any sequence splits),
+// the plan's work items and its two counters.
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits);
+// Where the plan lives inside that workspace.
+void decode_plan_layout(void *ws, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits,
+                        int4 **items, int **count);
 
-cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, int block_size, cudaStream_t stream, bool fp8 = false);
+// The plan launch (with the fused append's CTAs), then the persistent decode
+// kernel (and the merge when any sequence splits), all on `stream`.
+// tm_q: q as rows [S * Hq][d] bf16, boxes of 64 columns x G rows, 128-byte swizzle.
+cudaError_t launch_decode(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                          const DecodeArgs &a, int head_dim, int block_size, int num_sms, cudaStream_t stream,
+                          bool fp8 = false);
 
 // ------------------------------------------------------------- append ------
 cudaError_t launch_kv_append(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new,
                              const int32_t *slot_mapping, int num_tokens, int num_kv_heads,
                              int head_dim, int block_size, int num_blocks, __nv_bfloat16 *k_pool,
-                             __nv_bfloat16 *v_pool, int *err, int check_err_first,
+                             __nv_bfloat16 *v_pool, int *err, int check_err_first, int num_sms,
                              cudaStream_t stream);
 
 // Whole-block copies between pools (device or pinned host memory).
@@ -120,6 +140,7 @@ struct CheckArgs {
     const int32_t *prefix_lens;   // [S] or null
     int num_seqs, max_blocks, block_size, num_blocks, max_seq_len, max_q_len;
     int decode_rows;              // mixed step: sequences [0, decode_rows) own query row s
+    int decode_slots;             // fused append: slot_mapping[s] >= 0 must be position seq_lens[s]-1 of s
     int *err;
 };
 cudaError_t launch_index_check(const CheckArgs &a, cudaStream_t stream);

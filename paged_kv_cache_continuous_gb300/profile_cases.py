@@ -1,8 +1,9 @@
 """Single-kernel cases for profiling (ncu) and quick timing.
 
     python -m paged_kv_cache_continuous_gb300.profile_cases decode [num_seqs] [llama7b|long]
+    python -m paged_kv_cache_continuous_gb300.profile_cases decode_append [num_seqs]
     python -m paged_kv_cache_continuous_gb300.profile_cases prefill 4096 | 1024,1024,1024,1024
-    python -m paged_kv_cache_continuous_gb300.profile_cases append
+    python -m paged_kv_cache_continuous_gb300.profile_cases append [mixed|churn]
     python -m paged_kv_cache_continuous_gb300.profile_cases decode_fp8 [num_seqs]
     python -m paged_kv_cache_continuous_gb300.profile_cases rope [num_tokens]
     python -m paged_kv_cache_continuous_gb300.profile_cases copy [num_pairs]
@@ -42,6 +43,19 @@ def decode(num_seqs: int = 128, which: str = "llama7b"):
     print(f"decode {which} seqs={st.num_seqs} split={split} max_splits={nsplit} kv_bytes={kv}")
 
 
+def decode_append(num_seqs: int = 128):
+    """The Llama-7B-shaped decode step with its append fused (the bench's step)."""
+    shape, kp, vp, st = wl.llama7b_decode(pool_device="cuda", num_seqs=num_seqs)
+    q, kn, vn, sl = _d(st.q), _d(st.k_new), _d(st.v_new), _d(st.slot_mapping)
+    bt, lens = _d(st.block_table), _d(st.seq_lens)
+    ws = pa.workspace(shape, st.num_seqs, st.max_seq_len)
+    out = torch.empty_like(q)
+    for _ in range(4):
+        pa.decode_append(shape, q, kn, vn, sl, kp, vp, bt, lens, st.max_seq_len, out=out, ws=ws)
+    pa.check_device_error()
+    print(f"decode_append seqs={st.num_seqs}")
+
+
 def decode_fp8(num_seqs: int = 128):
     """The Llama-7B-shaped decode step over fp8 (e4m3) pools."""
     shape, _, _, st = wl.llama7b_decode(pool_device=None, num_seqs=num_seqs)
@@ -70,9 +84,21 @@ def prefill(prompts):
     print(f"prefill prompts={prompts}")
 
 
-def append():
-    shape, kp, vp, st = wl.mixed(pool_device="cuda")
-    kn, vn, sl = _d(st.k_new), _d(st.v_new), _d(st.slot_mapping)
+def append(which: str = "mixed"):
+    """The mixed step's rows (3196), or one churn step's (~13.6 K rows, B = 32)."""
+    if which == "churn":
+        ch = wl.Churn(pool_device="cuda", draw_values=False)
+        st = [ch.step() for _ in range(6)][-1]
+        shape = ch.shape
+        kp, vp = ch.initial_pool()
+        g = torch.Generator(device="cuda").manual_seed(3)
+        T = st.num_tokens
+        kn = torch.randn(T, shape.num_kv_heads, shape.head_dim, generator=g, device="cuda").to(torch.bfloat16)
+        vn = torch.randn_like(kn)
+        sl = _d(st.slot_mapping)
+    else:
+        shape, kp, vp, st = wl.mixed(pool_device="cuda")
+        kn, vn, sl = _d(st.k_new), _d(st.v_new), _d(st.slot_mapping)
     for _ in range(4):
         pa.kv_append(shape, kn, vn, sl, kp, vp)
     pa.check_device_error()
@@ -118,10 +144,12 @@ def main(argv):
     case = argv[1] if len(argv) > 1 else "decode"
     if case == "decode":
         decode(int(argv[2]) if len(argv) > 2 else 128, argv[3] if len(argv) > 3 else "llama7b")
+    elif case == "decode_append":
+        decode_append(int(argv[2]) if len(argv) > 2 else 128)
     elif case == "prefill":
         prefill([int(x) for x in (argv[2] if len(argv) > 2 else "4096").split(",")])
     elif case == "append":
-        append()
+        append(argv[2] if len(argv) > 2 else "mixed")
     elif case == "decode_fp8":
         decode_fp8(int(argv[2]) if len(argv) > 2 else 128)
     elif case == "rope":

@@ -104,17 +104,26 @@ def test_empty_calls_are_noops(lib):
     assert lib.pa_last_error() == b""
 
 
+def _ws_bytes(S, Hq, Hkv, d, splits):
+    """The documented workspace: split partials (fp32 acc and (max, sum) per
+    sequence, query head and split, rounded up to 16 bytes; none for one
+    split), then the plan's work items (16 bytes per sequence, split and KV
+    head) and its 16 bytes of counters."""
+    partials = -(-(S * Hq * splits * (d + 2) * 4) // 16) * 16 if splits > 1 else 0
+    return partials + S * splits * Hkv * 16 + 16
+
+
 def test_workspace_size(lib):
     sh = binding.PaShape(32, 8, 128, 16, 100, 0.0)
     n = ctypes.c_size_t()
     assert lib.pa_workspace_size(ctypes.byref(sh), 128, 256, ctypes.byref(n)) == 0
-    assert n.value == 0  # one split: no partials
+    assert n.value == _ws_bytes(128, 32, 8, 128, 1)  # one split: the plan only
     assert lib.pa_workspace_size(ctypes.byref(sh), 128, 2049, ctypes.byref(n)) == 0
     splits = -(-2049 // 256)
-    assert n.value == 128 * 32 * splits * (128 + 2) * 4
+    assert n.value == _ws_bytes(128, 32, 8, 128, splits)
     assert lib.pa_set_decode_split(64) == 0
     assert lib.pa_workspace_size(ctypes.byref(sh), 2, 2049, ctypes.byref(n)) == 0
-    assert n.value == 2 * 32 * (-(-2049 // 64)) * 130 * 4
+    assert n.value == _ws_bytes(2, 32, 8, 128, -(-2049 // 64))
     assert lib.pa_set_decode_split(0) == 0
     assert lib.pa_set_decode_split(-1) == binding.ERR_INVALID_ARG
     assert lib.pa_set_prefill_pairs(3) == 0

@@ -196,3 +196,90 @@ def test_llama7b_decode_full_size_sampled(cuda_lib):
 def test_long_context_full_size_sampled(cuda_lib):
     shape, kp, vp, st = wl.long_context(pool_device="cuda")
     _sampled_full_size(shape, kp, vp, st, np.random.default_rng(1), 48, "32 x 32K decode")
+
+
+# ------------------------------------------------ decode with fused append --
+@pytest.mark.parametrize("Hq,Hkv,d,B", [(32, 32, 128, 16), (32, 8, 128, 16), (64, 8, 128, 16), (32, 2, 128, 32),
+                                         (8, 4, 64, 16), (12, 4, 64, 32)])
+@pytest.mark.parametrize("split", [0, 64])
+def test_decode_append_matches_oracle(cuda_lib, Hq, Hkv, d, B, split):
+    """pa_decode_append = pa_kv_append of the step's rows, then pa_decode:
+    the pools bit for bit against the oracle's append, the outputs against
+    the oracle's decode over those pools."""
+    shape, kp, vp, st = _ragged(15, LENS, Hq, Hkv, d, B)
+    kd, vd = dev(kp), dev(vp)
+    pa.set_decode_split(split)
+    try:
+        out = pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), kd, vd,
+                               dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
+        pa.check_device_error()
+    finally:
+        pa.set_decode_split(0)
+    kq, vq = oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, bits(kp), bits(vp))
+    assert np.array_equal(bits(kd), kq) and np.array_equal(bits(vd), vq), "pools after the fused append"
+    ref = oracle.decode(bits(st.q), kq, vq, st.block_table, st.seq_lens)
+    assert_close(out, ref, f"decode_append G={Hq // Hkv} d={d} B={B} split={split}")
+
+
+def test_decode_append_padding_and_bad_slot(cuda_lib):
+    """Padding slots (< 0) write nothing; a slot past the pool is skipped and
+    flagged, every other row still lands and decodes."""
+    shape, kp, vp, st = _ragged(16, [40, 1, 300, 77], 16, 4, 128, 16)
+    slots = st.slot_mapping.copy()
+    slots[1] = -1
+    kd, vd = dev(kp), dev(vp)
+    pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(slots), kd, vd,
+                     dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
+    pa.check_device_error()
+    kq, vq = oracle.kv_append(bits(st.k_new), bits(st.v_new), slots, bits(kp), bits(vp))
+    assert np.array_equal(bits(kd), kq) and np.array_equal(bits(vd), vq), "padding slot"
+    bad = st.slot_mapping.copy()
+    bad[2] = shape.num_blocks * shape.block_size + 3
+    kd2, vd2 = dev(kp), dev(vp)
+    pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(bad), kd2, vd2,
+                     dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.check_device_error()
+    assert e.value.code == pa.ERR_BAD_INDEX
+    bad[2] = -1
+    kq2, vq2 = oracle.kv_append(bits(st.k_new), bits(st.v_new), bad, bits(kp), bits(vp))
+    assert np.array_equal(bits(kd2), kq2) and np.array_equal(bits(vd2), vq2), "rows beside a bad slot"
+
+
+def test_decode_append_validation_rejects_a_slot_off_the_last_position(cuda_lib):
+    shape, kp, vp, st = _ragged(17, [40, 70, 5], 8, 2, 128, 16)
+    slots = st.slot_mapping.copy()
+    slots[0], slots[1] = slots[1], slots[0]   # each a valid slot, of the wrong sequence
+    kd, vd = dev(kp), dev(vp)
+    out = torch.full((3, 8, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    pa.set_validation(True)
+    try:
+        pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(slots), kd, vd,
+                         dev(st.block_table), dev(st.seq_lens), st.max_seq_len, out=out)
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.check_device_error()
+    finally:
+        pa.set_validation(False)
+    assert e.value.code == pa.ERR_BAD_INDEX
+    assert torch.all(out == 7.0)
+    assert np.array_equal(bits(kd), bits(kp)) and np.array_equal(bits(vd), bits(vp)), "nothing written"
+
+
+def test_llama7b_decode_append_full_size_sampled(cuda_lib):
+    """The bench's step through pa_decode_append at full size: whole pools
+    against the oracle's append on a host snapshot, sampled outputs."""
+    shape, kd, vd, st = wl.llama7b_decode(pool_device="cuda")
+    kh, vh = bits(kd), bits(vd)
+    out = pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), kd, vd,
+                           dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
+    pa.check_device_error()
+    oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, kh, vh, inplace=True)
+    assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh), "pools after the fused append"
+    rng = np.random.default_rng(6)
+    seqs = sample(rng, st.num_seqs, 12)
+    kc, vc, bt = compact_pool(kh, vh, st.block_table, st.seq_lens, seqs, shape.block_size)
+    pairs = np.array([(i, int(h)) for i in range(len(seqs)) for h in rng.choice(32, 4, replace=False)],
+                     dtype=np.int32)
+    ref = oracle.decode(bits(st.q)[seqs], kc, vc, bt, st.seq_lens[seqs], pairs=pairs)
+    got = out[torch.tensor(seqs[pairs[:, 0]]), torch.tensor(pairs[:, 1])]
+    assert_close(got, ref, "Llama-7B decode_append")

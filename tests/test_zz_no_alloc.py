@@ -78,14 +78,16 @@ def test_noalloc_reuses_its_buffer_across_batches(cuda_lib):
 def test_noalloc_accepts_a_batch_above_the_workspace_bound(cuda_lib):
     """pa_workspace_size is an upper bound (it assumes the shortest split);
     the call checks the exact need of the plan it runs.  48 sequences of up
-    to 4096 tokens with 64 query heads: the bound is ~26 MB, the plan's need
-    (512-token splits) ~13 MB, so the call is accepted and must be right."""
+    to 4096 tokens with 64 query heads / 8 KV heads: the bound is ~26 MB, the
+    plan's need (512-token splits: partials and work items) ~13 MB, so the
+    call is accepted and must be right."""
     pa.set_decode_split(0)
     rng = np.random.default_rng(104)
     lens = [4096] + rng.integers(1, 4097, size=47).tolist()
     shape, kp, vp, st, ref = _batch(104, lens, Hq=64, Hkv=8)
     split, max_splits = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
-    need = st.num_seqs * 64 * max_splits * (128 + 2) * 4 if max_splits > 1 else 0
+    partials = st.num_seqs * 64 * max_splits * (128 + 2) * 4 if max_splits > 1 else 0
+    need = -(-partials // 16) * 16 + st.num_seqs * max(max_splits, 1) * 8 * 16 + 16  # + the plan's items
     assert pa.workspace_size(shape, st.num_seqs, st.max_seq_len) > SCRATCH >= need, (split, max_splits)
     out = pa.decode_noalloc(shape, dev(st.q), kp, vp, dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
     pa.check_device_error()
