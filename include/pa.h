@@ -144,23 +144,18 @@ int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool,
               void *stream);
 
 /*
- * Decode step with its append fused in: the same result as
+ * Decode step with its append fused in: exactly
  *     pa_kv_append(k_new, v_new, slot_mapping, num_seqs rows)
  *     followed by pa_decode(...)
- * in one launch (plus the merge).  Sequence s brings one new row,
+ * (the pages' decode step: the new token's key and value join the cache and
+ * the new token attends to all of it, text-generation-inference
+ * Router/Webserver deep dive, section "Prefill, Decode and past key
+ * values"), in fewer launches: the decode's planning launch (which lists the
+ * batch's work items) copies the rows too.  Sequence s brings one new row,
  * k_new[s] / v_new[s] ([S][Hkv][d]), whose slot is slot_mapping[s] (< 0:
- * none); the CTA that reads the sequence's last block writes the row there
- * first and orders that write before its own read of the block, so the row
- * is attended to without a separate pass over the new rows (the pages' decode
- * step: the new token's key and value join the cache and the new token
- * attends to all of it, text-generation-inference Router/Webserver deep
- * dive, section "Prefill, Decode and past key values").
- * Requirement (the router's allocator meets it): slot_mapping[s] >= 0 is the
- * slot of position seq_lens[s] - 1 of sequence s, i.e.
- * block_table[s][(L-1)/B] * B + (L-1) % B; in validation mode any other
- * slot sets PA_ERR_BAD_INDEX and nothing is written.  A slot past the pool
- * sets the error word and is skipped.  Arguments, workspace, errors and
- * asynchrony as pa_decode and pa_kv_append; bf16 pools only.
+ * none; slots distinct, as for pa_kv_append).  A slot past the pool sets the
+ * error word and is skipped.  Arguments, workspace, errors and asynchrony as
+ * pa_decode and pa_kv_append; bf16 pools only.
  */
 int pa_decode_append(const pa_shape_t *shape, const void *q, const void *k_new,
                      const void *v_new, const int32_t *slot_mapping, void *k_pool,
@@ -196,14 +191,13 @@ int pa_prefill(const pa_shape_t *shape, const void *q, const void *k,
  *      query row each (q_start_loc[s+1] - q_start_loc[s] == 1);
  *   3. causal prefill (paged form, prefix = seq_lens[s] - n_s) for sequences
  *      [num_decode, num_seqs).
- * Steps 2 and 3 run concurrently: the decode rows' append is fused into the
- * decode kernel (as pa_decode_append, so each decode row's slot must be its
- * sequence's last position), which starts at once on `stream`; the prompt
- * rows' append and the prefill go to a higher-priority stream owned by the
- * library (one per device, created on first use), forked from `stream` and
- * joined back into it with events, so work enqueued on `stream` afterwards
- * sees the whole step.  Blocks that one sequence writes in the step must not
- * be read by another (the allocator's ownership rule).
+ * Steps 2 and 3 run concurrently: the decode rows' append goes with the
+ * decode (as pa_decode_append) on `stream`; the prompt rows' append and the
+ * prefill go to a higher-priority stream owned by the library (one per
+ * device, created on first use), forked from `stream` and joined back into it
+ * with events, so work enqueued on `stream` afterwards sees the whole step.
+ * Blocks that one sequence writes in the step must not be read by another
+ * (the allocator's ownership rule).
  * q_start_loc [num_seqs+1] packs the rows of q/k_new/v_new/out; seq_lens counts
  * tokens after the append.  max_seq_len bounds seq_lens, max_q_len bounds the
  * prefill rows per sequence.  workspace as for pa_decode.

@@ -8,8 +8,8 @@
 // slot < 0 is padding.  A pure bit copy: 16-byte vector loads and stores,
 // consecutive threads on consecutive 16-byte pieces of one (token, head) row,
 // so both the read of k_new and the write into the pool are coalesced.
-// (Decode steps can instead append their rows inside the decode kernel:
-// pa_decode_append.)
+// (Decode steps can instead append their rows in the decode's planning
+// launch: pa_decode_append.)
 #include <algorithm>
 
 #include "pa_common.cuh"
@@ -156,17 +156,6 @@ __global__ void __launch_bounds__(256) index_check_kernel(const CheckArgs a) {
             for (int b = 0; b < nb; ++b) {
                 const int blk = a.block_table[(size_t)s * a.max_blocks + b];
                 if (blk < 0 || blk >= a.num_blocks) set_error(a.err, PA_ERR_BAD_INDEX);
-            }
-            // A fused append writes row s inside the decode of sequence s: its
-            // slot must be the sequence's last position (or padding).
-            if (a.decode_slots && a.slot_mapping && s < a.decode_rows) {
-                const int sl = a.slot_mapping[s];
-                const int p = L - 1;
-                if (sl >= 0 && (p < 0 || (long long)sl != (long long)a.block_table[(size_t)s * a.max_blocks +
-                                                                                    p / a.block_size] *
-                                                                                   a.block_size +
-                                                                               p % a.block_size))
-                    set_error(a.err, PA_ERR_BAD_INDEX);
             }
         }
     }

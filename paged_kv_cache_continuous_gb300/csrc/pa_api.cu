@@ -611,8 +611,6 @@ int pa_decode_append(const pa_shape_t *shape, const void *q, const void *k_new, 
         ca.block_size = shape->block_size;
         ca.num_blocks = shape->num_blocks;
         ca.max_seq_len = max_seq_len;
-        ca.decode_rows = num_seqs;
-        ca.decode_slots = 1;
         ca.err = d->err;
         if ((rc = run_check(ca, st))) return rc;
     }
@@ -827,7 +825,6 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
         ca.max_seq_len = max_seq_len;
         ca.max_q_len = max_q_len > 1 ? max_q_len : 1;
         ca.decode_rows = num_decode;
-        ca.decode_slots = 1;
         ca.err = d->err;
         if ((rc = run_check(ca, st))) return rc;
     }

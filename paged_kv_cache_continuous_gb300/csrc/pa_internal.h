@@ -41,7 +41,7 @@ struct DecodeArgs {
     float scale_log2;            // softmax scale * log2(e)
     const float *k_scale, *v_scale;  // fp8 pools: [Hkv] scales (value = code * scale); else null
     // Fused append (pa_decode_append; null otherwise): row s of k_new / v_new
-    // [S][Hkv][d] goes to slot_mapping[s] of the pools before it is read.
+    // [S][Hkv][d] goes to slot_mapping[s] of the pools, in the plan launch.
     const __nv_bfloat16 *k_new, *v_new;
     const int32_t *slot_mapping;
     __nv_bfloat16 *k_pool, *v_pool;
@@ -140,7 +140,6 @@ struct CheckArgs {
     const int32_t *prefix_lens;   // [S] or null
     int num_seqs, max_blocks, block_size, num_blocks, max_seq_len, max_q_len;
     int decode_rows;              // mixed step: sequences [0, decode_rows) own query row s
-    int decode_slots;             // fused append: slot_mapping[s] >= 0 must be position seq_lens[s]-1 of s
     int *err;
 };
 cudaError_t launch_index_check(const CheckArgs &a, cudaStream_t stream);

@@ -246,16 +246,33 @@ def test_decode_append_padding_and_bad_slot(cuda_lib):
     assert np.array_equal(bits(kd2), kq2) and np.array_equal(bits(vd2), vq2), "rows beside a bad slot"
 
 
-def test_decode_append_validation_rejects_a_slot_off_the_last_position(cuda_lib):
+def test_decode_append_is_append_then_decode_for_any_slots(cuda_lib):
+    """The rows go in before anything is read, so any distinct slots give
+    exactly pa_kv_append + pa_decode: here two sequences' new rows are
+    written into each other's last positions (the oracle appends the same)."""
     shape, kp, vp, st = _ragged(17, [40, 70, 5], 8, 2, 128, 16)
     slots = st.slot_mapping.copy()
-    slots[0], slots[1] = slots[1], slots[0]   # each a valid slot, of the wrong sequence
+    slots[0], slots[1] = slots[1], slots[0]
+    kd, vd = dev(kp), dev(vp)
+    out = pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(slots), kd, vd,
+                           dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
+    pa.check_device_error()
+    kq, vq = oracle.kv_append(bits(st.k_new), bits(st.v_new), slots, bits(kp), bits(vp))
+    assert np.array_equal(bits(kd), kq) and np.array_equal(bits(vd), vq)
+    ref = oracle.decode(bits(st.q), kq, vq, st.block_table, st.seq_lens)
+    assert_close(out, ref, "decode_append with exchanged slots")
+
+
+def test_decode_append_validation_mode_writes_nothing_on_a_bad_table(cuda_lib):
+    shape, kp, vp, st = _ragged(18, [40, 70, 5], 8, 2, 128, 16)
+    bt = st.block_table.copy()
+    bt[1, 1] = -4
     kd, vd = dev(kp), dev(vp)
     out = torch.full((3, 8, 128), 7.0, dtype=torch.bfloat16, device="cuda")
     pa.set_validation(True)
     try:
-        pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(slots), kd, vd,
-                         dev(st.block_table), dev(st.seq_lens), st.max_seq_len, out=out)
+        pa.decode_append(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), kd, vd,
+                         dev(bt), dev(st.seq_lens), st.max_seq_len, out=out)
         with pytest.raises(pa.PagedAttnError) as e:
             pa.check_device_error()
     finally:
