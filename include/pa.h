@@ -98,7 +98,8 @@ int pa_version(void);
  * pa_mixed_step for batches of at most max_seqs sequences whose lengths
  * (after the step's append) are at most max_seq_len.  The workspace holds the
  * decode plan (the batch's work items, one per sequence, KV head and split,
- * and two counters) and the split-K partial results (fp32); it is owned by
+ * its counters and 8 bytes per sequence) and the split-K partial results
+ * (fp32); it is owned by
  * the caller, its contents need no initialisation, and two calls whose
  * kernels may overlap on the GPU need two workspaces.  Writes *bytes.
  */
@@ -225,7 +226,7 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
  *  - A batch whose partials need more than the buffer holds is rejected
  *    with PA_ERR_WORKSPACE before anything is enqueued; use pa_decode then.
  *    The exact need, with max_splits from pa_decode_plan(shape, num_seqs,
- *    max_seq_len), is P + num_seqs * max_splits * Hkv * 16 + 16 bytes, where
+ *    max_seq_len), is P + num_seqs * (max_splits * Hkv * 16 + 8) + 16 bytes, where
  *    P = num_seqs * Hq * max_splits * (d + 2) * 4 rounded up to a multiple
  *    of 16 (P = 0 when max_splits is 1).  pa_workspace_size(shape, num_seqs,
  *    max_seq_len) is an upper bound of that need (it assumes the shortest

@@ -188,24 +188,37 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     const int start = block_excl_scan(threadIdx.x < kPlanBins ? bins[threadIdx.x] : 0, tmp, &total_last);
     if (threadIdx.x < kPlanBins) bins[threadIdx.x] = start;  // now the next free position of each size
     __syncthreads();
+    // Phase 1, a thread per sequence: where its items go (pf: its first full
+    // split's row of items, pos: its last split's place among the last
+    // splits), into a per-sequence array of the workspace.
     for (int s = s_beg; s < s_end; ++s) {
         const int L = a.seq_lens[s];
         const bool ok = len_ok(a, L, BS);
+        int2 at = make_int2(-1, -1);
         if (!ok || L == 0) {
             if (!ok) set_error(a.err, PA_ERR_BAD_INDEX);
             if (ok) {  // an empty context attends to nothing: zeros
                 uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)s * a.num_q_heads * D);
                 for (int i = 0; i < a.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
             }
-            continue;
+        } else {
+            const int ns = (L + split - 1) / split;
+            at = make_int2(pf, total_full + atomicAdd(&bins[key_of(L, ns)], 1));
+            pf += ns - 1;
         }
+        a.plan_seq[s] = at;
+    }
+    __syncthreads();
+    // Phase 2, a thread per (sequence, KV head), KV heads fastest: the items,
+    // so that neighbouring threads write neighbouring descriptors.
+    for (int p = threadIdx.x; p < S * Hkv; p += 1024) {
+        const int s = p / Hkv, g = p - s * Hkv;
+        const int2 at = a.plan_seq[s];
+        if (at.x < 0) continue;
+        const int L = a.seq_lens[s];
         const int ns = (L + split - 1) / split;
-        for (int c = 0; c < ns - 1; ++c)
-            for (int g = 0; g < Hkv; ++g) a.plan_items[(size_t)(pf + c) * Hkv + g] = make_int4(s, g, c, L);
-        pf += ns - 1;
-        const int pos = atomicAdd(&bins[key_of(L, ns)], 1);
-        for (int g = 0; g < Hkv; ++g)
-            a.plan_items[(size_t)(total_full + pos) * Hkv + g] = make_int4(s, g, ns - 1, L);
+        for (int c = 0; c < ns - 1; ++c) a.plan_items[(size_t)(at.x + c) * Hkv + g] = make_int4(s, g, c, L);
+        a.plan_items[(size_t)at.y * Hkv + g] = make_int4(s, g, ns - 1, L);
     }
     if (threadIdx.x == 0) a.plan_count[0] = (total_full + total_last) * Hkv;
 }
@@ -771,7 +784,7 @@ int decode_max_splits(int max_seq_len, int split_tokens) {
 
 // Layout: [part_acc S*Hq*max_splits*d floats][part_ml S*Hq*max_splits*2
 // floats] (only when max_splits > 1), then the plan, 16-byte aligned:
-// [items: S * max_splits * Hkv int4][count: 4 ints].
+// [items: S * max_splits * Hkv int4][count: 4 ints][per sequence: int2].
 static size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits) {
     if (max_splits <= 1) return 0;
     const size_t n = (size_t)num_seqs * num_q_heads * max_splits;
@@ -780,14 +793,17 @@ static size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int ma
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits) {
     return partials_bytes(num_seqs, num_q_heads, head_dim, max_splits) +
-           (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4) + 4 * sizeof(int);
+           (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4) + 4 * sizeof(int) +
+           (size_t)num_seqs * sizeof(int2);
 }
 
 void decode_plan_layout(void *ws, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits,
-                        int4 **items, int **count) {
+                        int4 **items, int **count, int2 **seq) {
     uint8_t *p = static_cast<uint8_t *>(ws) + partials_bytes(num_seqs, num_q_heads, head_dim, max_splits);
     *items = reinterpret_cast<int4 *>(p);
-    *count = reinterpret_cast<int *>(p + (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4));
+    p += (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4);
+    *count = reinterpret_cast<int *>(p);
+    *seq = reinterpret_cast<int2 *>(p + 4 * sizeof(int));
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,

@@ -51,6 +51,7 @@ struct DecodeArgs {
     // plan_count[0] = their number.
     int4 *plan_items;
     int *plan_count;
+    int2 *plan_seq;  // the plan's per-sequence scratch
 };
 
 // Tokens per split-K chunk chosen for a decode batch (multiple of block_size).
@@ -62,7 +63,7 @@ int decode_max_splits(int max_seq_len, int split_tokens);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits);
 // Where the plan lives inside that workspace.
 void decode_plan_layout(void *ws, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits,
-                        int4 **items, int **count);
+                        int4 **items, int **count, int2 **seq);
 
 // The plan launch (with the fused append's CTAs), then the persistent decode
 // kernel (and the merge when any sequence splits), all on `stream`.

@@ -108,9 +108,9 @@ def _ws_bytes(S, Hq, Hkv, d, splits):
     """The documented workspace: split partials (fp32 acc and (max, sum) per
     sequence, query head and split, rounded up to 16 bytes; none for one
     split), then the plan's work items (16 bytes per sequence, split and KV
-    head) and its 16 bytes of counters."""
+    head), its 16 bytes of counters and 8 bytes per sequence."""
     partials = -(-(S * Hq * splits * (d + 2) * 4) // 16) * 16 if splits > 1 else 0
-    return partials + S * splits * Hkv * 16 + 16
+    return partials + S * splits * Hkv * 16 + 16 + S * 8
 
 
 def test_workspace_size(lib):

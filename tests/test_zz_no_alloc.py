@@ -87,7 +87,7 @@ def test_noalloc_accepts_a_batch_above_the_workspace_bound(cuda_lib):
     shape, kp, vp, st, ref = _batch(104, lens, Hq=64, Hkv=8)
     split, max_splits = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
     partials = st.num_seqs * 64 * max_splits * (128 + 2) * 4 if max_splits > 1 else 0
-    need = -(-partials // 16) * 16 + st.num_seqs * max(max_splits, 1) * 8 * 16 + 16  # + the plan's items
+    need = -(-partials // 16) * 16 + st.num_seqs * (max(max_splits, 1) * 8 * 16 + 8) + 16  # + the plan
     assert pa.workspace_size(shape, st.num_seqs, st.max_seq_len) > SCRATCH >= need, (split, max_splits)
     out = pa.decode_noalloc(shape, dev(st.q), kp, vp, dev(st.block_table), dev(st.seq_lens), st.max_seq_len)
     pa.check_device_error()
