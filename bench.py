@@ -359,7 +359,10 @@ def load_traffic(kernel: str, nbytes, num_seqs):
         for name, key in (("decode.cu", "decode_cu_sha256"), ("pa_common.cuh", "pa_common_cuh_sha256")):
             if d.get(key) != hashlib.sha256((csrc / name).read_bytes()).hexdigest():
                 return None  # the kernel changed since the counters were taken
-        return d.get("dram_bytes_per_launch")
+        # the call's three launches: the decode kernel and the plan and merge
+        # launches beside it
+        other = sum(v.get("dram_bytes", 0) for v in d.get("other_launches_of_the_call", {}).values())
+        return d.get("dram_bytes_per_launch") + other
     except Exception:
         return None
 
