@@ -828,8 +828,8 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
         ca.err = d->err;
         if ((rc = run_check(ca, st))) return rc;
     }
-    // Decode rows [0, num_decode) are appended inside the decode kernel (each
-    // by the CTA that reads that sequence's last block); the prompt rows
+    // Decode rows [0, num_decode) are appended by the decode's plan launch,
+    // before its attention kernel reads anything; the prompt rows
     // [num_decode, num_tokens) by the append kernel ahead of the prefill.
     const int np = num_seqs - num_decode;
     const bool has_prefill = np > 0 && max_q_len > 0 && num_tokens > 0;
