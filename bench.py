@@ -217,7 +217,8 @@ def run_ours(args, world, rank, local):
         step()
     pa.check_device_error()
 
-    split, max_splits = pa.decode_plan(shape, st.num_seqs, max_len)
+    _, max_splits = pa.decode_plan(shape, st.num_seqs, max_len)
+    split = pa.planned_split(ws, shape, st.num_seqs, max_len)  # the split the plan launch took
     nbytes = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
     launches_per_step = 1 + (1 if max_splits > 1 else 0)
 
@@ -535,7 +536,7 @@ def measure_fp8_decode(pa, wl, dev, hbm_peak, steps):
     torch.cuda.synchronize(dev)
     pa.check_device_error()
     t = a.elapsed_time(b) / 1e3 / steps
-    split, _ = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
+    split = pa.planned_split(ws, shape, st.num_seqs, st.max_seq_len)
     nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
     fp8_bytes = nb["decode"] - nb["kv"] // 2
     return {"kernel": "decode_splitk_kernel<128,16,*,fp8> + decode_merge_kernel", "ms": round(t * 1e3, 5),
@@ -586,11 +587,12 @@ def measure_long_context(pa, wl, dev, hbm_peak, iters):
     slots, bt, lens = tod(st.slot_mapping), tod(st.block_table), tod(st.seq_lens)
     ws = pa.workspace(shape, st.num_seqs, st.max_seq_len, dev)
     out = torch.empty_like(q)
-    split, nsplit = pa.decode_plan(shape, st.num_seqs, st.max_seq_len)
-    nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
     t_app = time_each(dev, lambda: pa.kv_append(shape, kn, vn, slots, kp, vp), iters)
     t_dec = time_each(dev, lambda: pa.decode(shape, q, kp, vp, bt, lens, st.max_seq_len, out=out, ws=ws), iters)
     pa.check_device_error()
+    split = pa.planned_split(ws, shape, st.num_seqs, st.max_seq_len)
+    nsplit = -(-int(st.max_seq_len) // split)
+    nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
     del kp, vp
     return {"workload": "32 x 32768 cached tokens (+1), Hq 64 / Hkv 8, d 128, B 16",
             "kernel": "decode_splitk_kernel + decode_merge_kernel", "split_tokens": split, "splits": nsplit,
@@ -628,7 +630,7 @@ def measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, iters):
     t_pre = time_each(dev, lambda: pa.prefill(shape, qp, kp, vp, cup, st.max_q_len, block_table=btp, out=outp),
                       iters, flush)
     pa.check_device_error()
-    split, _ = pa.decode_plan(shape, nd, dmax)
+    split = pa.planned_split(ws, shape, nd, dmax)
     nb = decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)
     T = int(st.q_start_loc[-1])
     append_b = T * shape.num_kv_heads * shape.head_dim * 2 * 2 * 2 + 4 * T
@@ -675,9 +677,7 @@ def measure_churn(pa, wl, dev, hbm_peak, bf16_peak, warmup):
         rows_n = np.diff(st.q_start_loc)
         dev_steps.append((T, nd, tod(st.q_start_loc), tod(st.seq_lens), tod(st.slot_mapping), tod(st.block_table),
                           int(st.seq_lens.max()), int(rows_n[nd:].max()) if len(rows_n) > nd else 1))
-        split, _ = pa.decode_plan(shape, nd, int(st.seq_lens[:nd].max()))
-        bytes_dec.append(decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)["decode"]
-                         + T * shape.num_kv_heads * shape.head_dim * 8 + 4 * T)
+        bytes_dec.append(T * shape.num_kv_heads * shape.head_dim * 8 + 4 * T)  # + the decode's, below
         n = rows_n[nd:].tolist()
         flops_pre.append(causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim))
         rows_pre.append(int(sum(n)))
@@ -697,6 +697,16 @@ def measure_churn(pa, wl, dev, hbm_peak, bf16_peak, warmup):
     torch.cuda.synchronize(dev)
     pa.check_device_error()
     t = np.array([a.elapsed_time(b) for a, b in ev]) / 1e3
+    # Accounting pass (untimed): each step again, then the split its plan
+    # launch took, for the decode's algorithmic bytes (the rows appended again
+    # are the same rows to the same slots).
+    for i, st in enumerate(steps):
+        run(i)
+        torch.cuda.synchronize(dev)
+        nd = st.num_decode
+        split = pa.planned_split(ws, shape, nd, dev_steps[i][6])
+        bytes_dec[i] += decode_step_bytes(shape, st.seq_lens[:nd], split, shape.block_size)["decode"]
+    pa.check_device_error()
     bound = np.maximum(np.array(bytes_dec) / (hbm_peak * 1e9), np.array(flops_pre) / (bf16_peak * 1e12))
     del kp, vp
     return {"workload": "512 seqs, log-uniform context [1,8192], Hq 32 / Hkv 8, d 128, B 32, 64 steps, 10 % "
@@ -815,7 +825,9 @@ def run_reference(args, world, rank):
     for _ in range(args.steps):
         oracle_step(oracle, shape, kp_h, vp_h, st, seqs, threads)
     t = time.perf_counter() - t0
-    b = decode_step_bytes(shape, st.seq_lens[seqs], 512, shape.block_size)["step"] * args.steps
+    # the bytes of the step without split partials (the oracle makes none; the
+    # GPU arm counts the few its plan launch makes)
+    b = decode_step_bytes(shape, st.seq_lens[seqs], 1 << 30, shape.block_size)["step"] * args.steps
     v = b / t / 1e9
     sample = (f"each step: append + decode of the first {len(seqs)} of {st.num_seqs} sequences "
               f"({int(st.seq_lens[seqs].sum())} context tokens), fp64 oracle")

@@ -110,10 +110,15 @@ int pa_workspace_size(const pa_shape_t *shape, int max_seqs, int max_seq_len,
  * Split-K plan of a decode batch (host side, first step of the path): the
  * tokens per split (a multiple of block_size) and the number of splits of the
  * longest sequence, for num_seqs sequences of at most max_seq_len tokens on
- * the current device (its SM count enters the choice).  Sequence s then uses
- * ceil(seq_lens[s] / split_tokens) splits (1 if it is empty); a sequence with
- * one split writes its output directly, the others go through the merge.
- * pa_decode and pa_mixed_step use exactly this plan.
+ * the current device (its SM count enters the choice).  This is the finest
+ * split the decode uses: its plan launch, which sees the batch's lengths,
+ * takes split_tokens * 2^k instead (k <= 5) when that still leaves at least
+ * six work items per decode CTA and no item longer than half of a CTA's share
+ * of the tokens -- fewer, longer items cost less.  Sequence s then uses
+ * ceil(seq_lens[s] / split) splits (1 if it is empty), never more than
+ * max_splits; a sequence with one split writes its output directly, the
+ * others go through the merge.  With pa_set_decode_split in effect the split
+ * is exactly the override.
  */
 int pa_decode_plan(const pa_shape_t *shape, int num_seqs, int max_seq_len,
                    int *split_tokens, int *max_splits);
@@ -333,7 +338,8 @@ const char *pa_last_error(void);
 
 /*
  * Decode split override (tokens per split; a multiple of block_size), for
- * tests comparing split and unsplit results.  0 restores the automatic choice.
+ * tests comparing split and unsplit results: the decode then uses exactly this
+ * split.  0 restores the automatic choice.
  */
 int pa_set_decode_split(int tokens);
 

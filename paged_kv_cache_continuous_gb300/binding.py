@@ -173,6 +173,17 @@ def decode_plan(shape, num_seqs: int, max_seq_len: int) -> tuple[int, int]:
     return a.value, b.value
 
 
+def planned_split(ws: torch.Tensor, shape, num_seqs: int, max_seq_len: int) -> int:
+    """Tokens per split that the last decode of (num_seqs, max_seq_len) with
+    workspace `ws` used (its plan launch may take a multiple of decode_plan's
+    split): the plan's second counter, after the partials and the items."""
+    _, max_splits = decode_plan(shape, num_seqs, max_seq_len)
+    n = num_seqs * shape.num_q_heads * max_splits
+    partials = ((n * shape.head_dim * 4 + n * 2 * 4 + 15) & ~15) if max_splits > 1 else 0
+    at = partials + num_seqs * max(max_splits, 1) * shape.num_kv_heads * 16
+    return int(ws[at + 4:at + 8].cpu().view(torch.int32)[0])
+
+
 def workspace(shape, max_seqs: int, max_seq_len: int, device="cuda") -> torch.Tensor:
     """A caller-owned workspace buffer of the size pa_workspace_size reports."""
     n = workspace_size(shape, max_seqs, max_seq_len)

@@ -142,10 +142,13 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     // anything this grid writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (a.check_err_first && *(volatile int *)a.err != 0) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) a.plan_count[0] = 0;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            a.plan_count[0] = 0;
+            a.plan_count[1] = a.split_tokens;
+        }
         return;
     }
-    const int S = a.num_seqs, split = a.split_tokens, Hkv = a.num_kv_heads;
+    const int S = a.num_seqs, Hkv = a.num_kv_heads;
     if (blockIdx.x > 0) {
         constexpr int NV = D / 8;  // 16-byte pieces per row
         const long long total = (long long)S * Hkv * NV;
@@ -168,13 +171,61 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
         }
         return;
     }
-    const int nbins = min(kPlanBins, (split + BS - 1) / BS);
-    // key 0 = the longest last split (nbins blocks or more)
-    auto key_of = [&](int L, int ns) { return nbins - min(nbins, (L - (ns - 1) * split + BS - 1) / BS); };
-    if (threadIdx.x < kPlanBins) bins[threadIdx.x] = 0;
-    __syncthreads();
     const int per = (S + 1023) / 1024;
     const int s_beg = min(S, (int)threadIdx.x * per), s_end = min(S, s_beg + per);
+    // The tokens per split: the host's choice, or (split_adapt) the largest
+    // split_tokens * 2^k, k <= kSplitGrowth, that still leaves at least
+    // kMinItemsPerCta items per decode CTA and no item longer than half of a
+    // CTA's share of the batch's tokens.  Each item costs a fixed overhead
+    // (its query rows, the merge of the four warps' states) besides its
+    // blocks, so fewer, longer items are faster as long as the CTAs stay
+    // evenly loaded.
+    int split = a.split_tokens;
+    if (a.split_adapt) {
+        constexpr int kSplitGrowth = 5, kMinItemsPerCta = 6;
+        long long cnt[kSplitGrowth + 1] = {}, tok = 0;
+        for (int s = s_beg; s < s_end; ++s) {
+            const int L = a.seq_lens[s];
+            if (!len_ok(a, L, BS) || L == 0) continue;
+            tok += L;
+#pragma unroll
+            for (int k = 0; k <= kSplitGrowth; ++k) cnt[k] += (L + (split << k) - 1) / (split << k);
+        }
+        __shared__ long long red[kSplitGrowth + 2][32];
+        auto block_sum = [&](long long v, int slot) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if ((threadIdx.x & 31) == 0) red[slot][threadIdx.x >> 5] = v;
+        };
+#pragma unroll
+        for (int k = 0; k <= kSplitGrowth; ++k) block_sum(cnt[k], k);
+        block_sum(tok, kSplitGrowth + 1);
+        __syncthreads();
+        __shared__ int chosen;
+        if (threadIdx.x < 32) {  // warp 0: the totals (lane k holds slot k), then the choice
+            long long t = 0;
+            if (threadIdx.x < kSplitGrowth + 2)
+                for (int w = 0; w < 32; ++w) t += red[threadIdx.x][w];
+            const long long tok_all = __shfl_sync(0xffffffffu, t, kSplitGrowth + 1);
+            const long long ctas = max(a.num_ctas, 1);
+            const long long sp = (long long)a.split_tokens << threadIdx.x;
+            // lane k >= 1 qualifies if its split still leaves enough, short enough items
+            const bool fits = threadIdx.x >= 1 && threadIdx.x <= kSplitGrowth && t * Hkv >= kMinItemsPerCta * ctas &&
+                              sp * 2 * ctas <= tok_all * Hkv;
+            // the largest k such that every k' <= k qualifies
+            const unsigned bad = __ballot_sync(0xffffffffu, !fits && threadIdx.x >= 1 && threadIdx.x <= kSplitGrowth);
+            const int kmax = bad ? __ffs(bad) - 2 : kSplitGrowth;  // first failing k, minus one
+            if (threadIdx.x == 0) chosen = a.split_tokens << kmax;
+        }
+        __syncthreads();
+        split = chosen;
+    }
+    const int nbins = min(kPlanBins, (split + BS - 1) / BS);
+    const int bw = ((split + BS - 1) / BS + nbins - 1) / nbins;  // blocks per bin
+    // key 0 = the longest last split
+    auto key_of = [&](int L, int ns) { return nbins - min(nbins, ((L - (ns - 1) * split + BS - 1) / BS + bw - 1) / bw); };
+    if (threadIdx.x < kPlanBins) bins[threadIdx.x] = 0;
+    __syncthreads();
     int nfull = 0;
     for (int s = s_beg; s < s_end; ++s) {
         const int L = a.seq_lens[s];
@@ -220,7 +271,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
         for (int c = 0; c < ns - 1; ++c) a.plan_items[(size_t)(at.x + c) * Hkv + g] = make_int4(s, g, c, L);
         a.plan_items[(size_t)at.y * Hkv + g] = make_int4(s, g, ns - 1, L);
     }
-    if (threadIdx.x == 0) a.plan_count[0] = (total_full + total_last) * Hkv;
+    if (threadIdx.x == 0) {
+        a.plan_count[0] = (total_full + total_last) * Hkv;
+        a.plan_count[1] = split;
+    }
 }
 
 // One work item as a warp holds it.
@@ -230,7 +284,7 @@ struct Item {
 };
 
 template <int BS>
-__device__ __forceinline__ Item load_item(const DecodeArgs &a, int k, int num_items) {
+__device__ __forceinline__ Item load_item(const DecodeArgs &a, int k, int num_items, int split) {
     Item it;
     it.valid = k < num_items;
     const int4 v = it.valid ? a.plan_items[k] : make_int4(0, 0, 0, 0);
@@ -238,9 +292,9 @@ __device__ __forceinline__ Item load_item(const DecodeArgs &a, int k, int num_it
     it.g = v.y;
     it.c = v.z;
     it.L = v.w;
-    it.nsplit = it.valid ? (it.L + a.split_tokens - 1) / a.split_tokens : 1;
-    it.t0 = it.c * a.split_tokens;
-    it.t1 = min(it.L, it.t0 + a.split_tokens);
+    it.nsplit = it.valid ? (it.L + split - 1) / split : 1;
+    it.t0 = it.c * split;
+    it.t1 = min(it.L, it.t0 + split);
     it.nblk = it.valid ? (it.t1 - it.t0 + BS - 1) / BS : 0;  // t0 is block aligned
     return it;
 }
@@ -282,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (*(volatile int *)s_abort) return;
 
-    const int num_items = a.plan_count[0];
+    const int num_items = a.plan_count[0], split = a.plan_count[1];
     const int nctas = gridDim.x;
     auto item_at = [&](int j) {  // the CTA's j-th item (snake order over the list)
         const int k = j * nctas + ((j & 1) ? nctas - 1 - (int)blockIdx.x : (int)blockIdx.x);
-        return load_item<BS>(a, k, num_items);
+        return load_item<BS>(a, k, num_items, split);
     };
 
     // ---------------------------------------------------------- producer --
@@ -684,7 +738,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     if (a.check_err_first && *(volatile int *)a.err != 0) return;
     const int L = a.seq_lens[s];
     if (L < 0 || L > a.max_seq_len) return;
-    const int nsplit = L > 0 ? (L + a.split_tokens - 1) / a.split_tokens : 1;
+    const int split = a.plan_count[1];  // the plan's choice
+    const int nsplit = L > 0 ? (L + split - 1) / split : 1;
     if (nsplit <= 1) return;
     const size_t p0 = ((size_t)s * a.num_q_heads + h) * a.max_splits;
     const float *ml = a.part_ml + p0 * 2;
@@ -728,20 +783,22 @@ cudaError_t launch_decode_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, co
     cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(decode_splitk_kernel<D, BS, BIG_G, FP8>),
                                 C::kSmemBytes, opted);
     if (e != cudaSuccess) return e;
-    // the plan's CTA, plus CTAs for the fused append (up to one per SM)
-    int plan_ctas = 1;
-    if (a.k_new) {
-        const long long pieces = (long long)a.num_seqs * a.num_kv_heads * (D / 8);
-        plan_ctas += (int)std::min<long long>(std::max(num_sms, 1), (pieces + 1023) / 1024);
-    }
-    decode_plan_kernel<D, BS><<<plan_ctas, 1024, 0, stream>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     // Persistent: as many CTAs per SM as fit, fewer when the items (counted
     // on the device; at most every split of every sequence) cannot fill them.
     const long long bound = (long long)a.num_seqs * a.num_kv_heads * a.max_splits;
     const long long ctas =
         std::max(1LL, std::min<long long>((long long)C::kCtasPerSm * std::max(num_sms, 1), bound));
+    DecodeArgs b = a;
+    b.num_ctas = (int)ctas;
+    // the plan's CTA, plus CTAs for the fused append (up to one per SM)
+    int plan_ctas = 1;
+    if (b.k_new) {
+        const long long pieces = (long long)b.num_seqs * b.num_kv_heads * (D / 8);
+        plan_ctas += (int)std::min<long long>(std::max(num_sms, 1), (pieces + 1023) / 1024);
+    }
+    decode_plan_kernel<D, BS><<<plan_ctas, 1024, 0, stream>>>(b);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     // Programmatic dependent launches: each kernel's CTAs are placed while
     // the previous one still runs and wait for it in griddepcontrol.wait, so
     // the launch gaps between the three kernels overlap the work.
@@ -755,12 +812,12 @@ cudaError_t launch_decode_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, co
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_splitk_kernel<D, BS, BIG_G, FP8>, tm_q, tm_k, tm_v, a);
-    if (e != cudaSuccess || a.max_splits <= 1) return e;
-    cfg.gridDim = dim3((a.num_q_heads + 3) / 4, a.num_seqs);
+    e = cudaLaunchKernelEx(&cfg, decode_splitk_kernel<D, BS, BIG_G, FP8>, tm_q, tm_k, tm_v, b);
+    if (e != cudaSuccess || b.max_splits <= 1) return e;
+    cfg.gridDim = dim3((b.num_q_heads + 3) / 4, b.num_seqs);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a);
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, b);
 }
 
 }  // namespace

@@ -224,9 +224,10 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
     const bool fp8 = k_scale != nullptr;
     // split_planned > 0: the caller has already planned the split (and sized
     // its scratch from it); the override is not read a second time.
+    const int override_tokens = g_split_override.load();
     const int split = split_planned > 0 ? split_planned
                                         : decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len,
-                                                              sh->block_size, d->num_sms, g_split_override.load());
+                                                              sh->block_size, d->num_sms, override_tokens);
     const int max_splits = decode_max_splits(max_seq_len, split);
     const size_t need = decode_workspace_bytes(num_seqs, sh->num_q_heads, sh->num_kv_heads, sh->head_dim,
                                                max_splits);
@@ -264,6 +265,7 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
     a.num_blocks = sh->num_blocks;
     a.max_blocks = max_blocks;
     a.split_tokens = split;
+    a.split_adapt = override_tokens > 0 ? 0 : 1;  // an override (tests) is taken exactly
     a.max_splits = max_splits;
     a.max_seq_len = max_seq_len;
     a.check_err_first = check_first;

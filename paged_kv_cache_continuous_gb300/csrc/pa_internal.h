@@ -37,6 +37,10 @@ struct DecodeArgs {
     int *err;                    // device error word
     int num_seqs, num_q_heads, num_kv_heads, group, num_blocks, max_blocks;
     int split_tokens, max_splits, max_seq_len;
+    // split_adapt: the plan launch may take split_tokens * 2^k instead (never
+    // more splits than max_splits allows), from the batch's actual lengths;
+    // the split it uses is plan_count[1].  num_ctas: the decode kernel's grid.
+    int split_adapt, num_ctas;
     int check_err_first;         // validation mode: skip work if *err != 0
     float scale_log2;            // softmax scale * log2(e)
     const float *k_scale, *v_scale;  // fp8 pools: [Hkv] scales (value = code * scale); else null
@@ -47,8 +51,8 @@ struct DecodeArgs {
     __nv_bfloat16 *k_pool, *v_pool;
     long long num_slots;
     // The plan (first step of the path): decode_plan_kernel writes the work
-    // items -- (sequence, KV head, split, length) -- into the workspace and
-    // plan_count[0] = their number.
+    // items -- (sequence, KV head, split, length) -- into the workspace,
+    // plan_count[0] = their number and plan_count[1] = the tokens per split.
     int4 *plan_items;
     int *plan_count;
     int2 *plan_seq;  // the plan's per-sequence scratch

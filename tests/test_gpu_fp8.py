@@ -32,7 +32,8 @@ def _case(seed, lens, Hq, Hkv, B, d=128):
     return shape, st, kp0, vp0, q
 
 
-@pytest.mark.parametrize("Hq,Hkv,B", [(32, 8, 16), (32, 32, 16), (64, 4, 32)])
+@pytest.mark.parametrize("Hq,Hkv,B", [(32, 8, 16), (32, 32, 16), (64, 4, 32), (64, 8, 16), (16, 8, 32), (40, 8, 16),
+                                      (24, 8, 32)])
 def test_fp8_append_and_decode(cuda_lib, Hq, Hkv, B):
     lens = [1, 15, 16, 17, 255, 700, 2049]
     shape, st, kp0, vp0, q = _case(Hq + B, lens, Hq, Hkv, B)
