@@ -63,10 +63,14 @@ struct DecodeCfg {
     static constexpr int kHalfBytes = BS * 128;            // one box: BS rows x 128 B
     static constexpr int kKVBytes = kHalves * kHalfBytes;  // K (or V) of one block
     static constexpr int kStageBytes = 2 * kKVBytes;
-    // 64 KB of blocks in flight per CTA.  A multiple of the consumer warps:
-    // stage st is read only by warp st % 4, block after block, so a warp
-    // never waits on a stage's barrier more than one phase ahead.
-    static constexpr int kStages = (65536 / kStageBytes) / kConsumerWarps * kConsumerWarps;
+    // 96 KB of blocks in flight per CTA (64 KB for G > 8, whose larger merge
+    // scratch would otherwise leave room for one CTA per SM): more bytes in
+    // flight than the DRAM latency needs, with room to spare for the short
+    // stalls of the consumers.  A multiple of the consumer warps: stage st is
+    // read only by warp st % 4, block after block, so a warp never waits on
+    // a stage's barrier more than one phase ahead.
+    static constexpr int kRingBudget = BIG_G ? 65536 : 98304;
+    static constexpr int kStages = (kRingBudget / kStageBytes) / kConsumerWarps * kConsumerWarps;
     static constexpr int kKSteps = D / 16;                 // QK^T k-steps
     static constexpr int kNTiles = D / 8;                  // PV n-tiles
     static constexpr int kRingBytes = kStages * kStageBytes;
@@ -83,6 +87,7 @@ struct DecodeCfg {
     // two: a third would need the registers cut to 128 (spills; measured slower)
     static constexpr int kCtasPerSm = 232448 / (kSmemBytes + 1024) < 2 ? 232448 / (kSmemBytes + 1024) : 2;
     static_assert(kStages >= kConsumerWarps && kStages < kQLane, "one producer lane per stage, and the q lane");
+    static_assert(kCtasPerSm == 2, "two CTAs per SM");
 };
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
@@ -554,10 +559,13 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                     m_run[rr] = mn;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) x[e] = fast_exp2(x[e] - mn);
+                    // the running maximum rarely moves after the first blocks
+                    if (__any_sync(0xffffffffu, alpha[rr] != 1.f)) {
 #pragma unroll
-                    for (int nt = 0; nt < C::kNTiles; ++nt) {
-                        acc[nt][rr * 2 + 0] *= alpha[rr];
-                        acc[nt][rr * 2 + 1] *= alpha[rr];
+                        for (int nt = 0; nt < C::kNTiles; ++nt) {
+                            acc[nt][rr * 2 + 0] *= alpha[rr];
+                            acc[nt][rr * 2 + 1] *= alpha[rr];
+                        }
                     }
                     p[0][rr * 2 + 0] = x[0];
                     p[0][rr * 2 + 1] = x[1];
