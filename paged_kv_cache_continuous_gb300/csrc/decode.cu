@@ -516,11 +516,11 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int ks = 2 * kp + u;
-                            const uint32_t lo = u ? b01 : b00, hi = u ? b11 : b10;
-                            mma_f16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(lo),
-                                          e4m3x2_to_f16x2(lo >> 16));
-                            mma_f16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(hi),
-                                          e4m3x2_to_f16x2(hi >> 16));
+                            uint32_t l0, l1, h0, h1;
+                            e4m3x4_to_f16x2x2(u ? b01 : b00, l0, l1);
+                            e4m3x4_to_f16x2x2(u ? b11 : b10, h0, h1);
+                            mma_f16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], l0, l1);
+                            mma_f16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], h0, h1);
                         }
                     }
                 } else {
@@ -602,14 +602,12 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                         ldmatrix_x4_trans(addr, v0, v1, v2, v3);
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const uint32_t lo = u ? v2 : v0, hi = u ? v3 : v1;
-#pragma unroll
-                            for (int par = 0; par < 2; ++par) {
-                                const uint32_t sel = par ? 0x3131u : 0x2020u;  // bytes (1, 3) or (0, 2)
-                                mma_f16_16816(acc[4 * jp + 2 * u + par], pa0, pa1, pa2, pa3,
-                                              e4m3x2_to_f16x2(__byte_perm(lo, 0u, sel)),
-                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, sel)));
-                            }
+                            // bytes (0, 2) -- the even d -- into the low half, (1, 3) into the high half
+                            uint32_t le, lo_, he, ho;
+                            e4m3x4_to_f16x2x2(__byte_perm(u ? v2 : v0, 0u, 0x3120u), le, lo_);
+                            e4m3x4_to_f16x2x2(__byte_perm(u ? v3 : v1, 0u, 0x3120u), he, ho);
+                            mma_f16_16816(acc[4 * jp + 2 * u + 0], pa0, pa1, pa2, pa3, le, he);
+                            mma_f16_16816(acc[4 * jp + 2 * u + 1], pa0, pa1, pa2, pa3, lo_, ho);
                         }
                     }
                 } else {

@@ -208,11 +208,12 @@ __device__ __forceinline__ float f16x2_sum(uint32_t v) {
     return lo + hi;
 }
 
-// Two e4m3 codes (low byte = first) -> two fp16 (exact; low half = first).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(two_codes));
-    return r;
+// Four e4m3 codes -> two fp16 pairs: codes 0, 1 into lo, codes 2, 3 into hi
+// (exact).  The 16-bit halves feed the conversions directly, without shifts.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
 }
 
 // Two floats -> two e4m3 codes (nearest even, saturating at +-448; low byte = lo).
