@@ -676,6 +676,17 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
             }
         };
         auto csync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); };
+        // The same barrier, true in every consumer thread if p holds in any.
+        auto csync_any = [&](bool p) {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+                "bar.red.or.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+                : "=r"(r)
+                : "r"((uint32_t)p), "n"(kConsumerWarps * 32)
+                : "memory");
+            return r != 0u;
+        };
         // two steps: warps 1 and 3 into 0 and 2, then 2 into 0
         csync();  // every warp is done with the item; the previous merge's reads are done
         if (warp & 1) put(warp >> 1);
@@ -725,11 +736,14 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                 }
             }
         }
-        // every consumer warp takes the same number of barriers, and leaves
-        // together once a wait has failed
-        if (!ok) atomicExch(s_abort, 1);
-        csync();
-        if (*(volatile int *)s_abort) break;
+        // Every consumer warp takes the same barriers, and all leave together
+        // once a wait has failed here or anywhere in the CTA: one barrier
+        // reduction decides it for all (a flag read after a plain barrier
+        // could change between the warps' reads).
+        if (csync_any(!ok || *(volatile int *)s_abort != 0)) {
+            if (!ok) atomicExch(s_abort, 1);
+            break;
+        }
     }
 }
 
