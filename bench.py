@@ -507,6 +507,37 @@ def measure_rope(pa, wl, dev, hbm_peak, iters):
         nbytes = T * (Hq + 2 * Hkv) * 128 * 2 * 2 + 8 * T
         res[name] = {"tokens": T, "ms": round(t * 1e3, 4), "GBps": round(nbytes / t / 1e9, 1),
                      "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 4)}
+        if name == "prompt_4096":
+            # Back to back over four input sets (4 x ~100 MB > L2, so every
+            # launch reads and writes DRAM), one event pair around all launches:
+            # the rate a serving loop's consecutive steps see, launch gaps
+            # included, without the per-launch flush and events.
+            sets = [(q, k, v, pos, slots, kp, vp, q_out)]
+            for j in range(3):
+                g2 = torch.Generator().manual_seed(31 + j)
+                sets.append((wl.bf16_randn((T, Hq, 128), g2).to(dev), wl.bf16_randn((T, Hkv, 128), g2).to(dev),
+                             wl.bf16_randn((T, Hkv, 128), g2).to(dev), pos,
+                             torch.randperm(nb * 16, generator=g2)[:T].to(torch.int32).to(dev),
+                             torch.zeros_like(kp), torch.zeros_like(vp), torch.empty_like(q)))
+            for st_ in sets:
+                pa.rope_append(shape, *st_[:5], st_[5], st_[6], q_out=st_[7])
+            torch.cuda.synchronize(dev)
+            n_l = max(4 * iters, 40)
+            torch.cuda._sleep(int(2e6 + 2e5 * n_l))  # the launches queue up before the GPU reaches them
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for j in range(n_l):
+                st_ = sets[j % 4]
+                pa.rope_append(shape, *st_[:5], st_[5], st_[6], q_out=st_[7])
+            b.record()
+            torch.cuda.synchronize(dev)
+            pa.check_device_error()
+            t2 = a.elapsed_time(b) / 1e3 / n_l
+            res["prompt_4096_back_to_back"] = {
+                "tokens": T, "ms": round(t2 * 1e3, 4), "GBps": round(nbytes / t2 / 1e9, 1),
+                "frac_hbm": round(nbytes / t2 / 1e9 / hbm_peak, 4), "launches": n_l,
+                "l2": "four input sets of ~100 MB in turn (inputs larger than L2); no flush"}
+            del sets
     return {"kernel": "rope_append_kernel", "l2": "flushed (256 MB write) before each launch", **res}
 
 

@@ -51,7 +51,11 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ float2 cs[kTok][72];
     __shared__ int s_slot[kTok];     // the token's slot, or -1 if it is not appended (or skipped)
     __shared__ int s_pos_ok[kTok];
+    // Under a programmatic dependent launch: the previous kernel's writes (the
+    // inputs) are visible past this point.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (a.check_err_first && *(volatile int *)a.err != 0) return;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int d = a.head_dim, half = d / 2;
     const int cpr = half / 8;  // 16-byte chunks per half row
     const long long num_slots = (long long)a.num_blocks * a.block_size;
@@ -143,8 +147,18 @@ cudaError_t launch_rope_append(const RopeArgs &a, int num_sms, cudaStream_t stre
     const int tpc = a.num_tokens >= num_sms * 8 ? kTok : 1;
     const int chunks = (a.num_tokens + tpc - 1) / tpc;
     const int blocks = std::max(1, std::min(chunks, num_sms * 8));
-    rope_append_kernel<<<blocks, kThreads, 0, stream>>>(a, tpc);
-    return cudaGetLastError();
+    // A programmatic dependent launch: the CTAs may be placed while the
+    // previous kernel on the stream finishes; they wait for it before reading.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rope_append_kernel, a, tpc);
 }
 
 }  // namespace pa
