@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(256)
                      const int32_t *__restrict__ slot_mapping, int num_vec, int num_kv_heads, int block_size,
                      long long num_slots, uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int *err,
                      int check_err_first) {
+    // A kernel launched after this one as a programmatic dependent (the
+    // prefill) may be placed now; it waits for this grid before reading.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (check_err_first && *(volatile int *)err != 0) return;
     const int step = gridDim.x * (256 * kAppendU);
     for (int base = blockIdx.x * (256 * kAppendU) + threadIdx.x; base < num_vec; base += step) {

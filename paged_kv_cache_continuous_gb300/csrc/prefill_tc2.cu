@@ -266,6 +266,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // alternating directions, which evens out the pairs' total work.
     auto unit_of = [&](int rnd) { return rnd * pairs + ((rnd & 1) ? pairs - 1 - pair : pair); };
 
+    // Under a programmatic dependent launch the CTAs are placed while the
+    // previous kernel on the stream finishes (e.g. the append that writes the
+    // prompt rows' K/V): nothing is read from global memory before its writes
+    // are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // The schedule (identical in both CTAs): each sequence's level count
     // (key), the number of sequences above each level, and the sequences
     // ordered by key, most first (stable, so both CTAs agree).
@@ -939,9 +946,17 @@ cudaError_t launch_pair_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, cons
                             (a.num_q_heads / heads_per_pair(MODE)) * a.num_seqs;
     if (units == 0) return cudaSuccess;
     const int pairs = (int)std::min<long long>(units, std::max(1, a.num_sms / 2));
-    prefill_pair_kernel<BS, PAGED, MODE><<<dim3(2 * pairs), kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_o,
-                                                                                        a);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];  // a programmatic dependent launch (the kernel waits before reading)
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<BS, PAGED, MODE>, tm_q, tm_k, tm_v, tm_o, a);
 }
 
 template <int BS, bool PAGED>
