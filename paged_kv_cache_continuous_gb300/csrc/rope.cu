@@ -24,7 +24,8 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTok = 4;    // tokens per CTA pass: their cos / sin first, then all their rows at once
+constexpr int kTok = 2;    // tokens per CTA pass: their cos / sin first, then all their rows at once
+                           // (two rather than four: 20.0 against 20.2 us for a 4096-token step)
 constexpr int kItems = 4;  // work items a thread holds in registers at once
 
 // Rotate eight pairs (i .. i+7 with i+d/2 .. i+d/2+7) of one head row: lo / hi
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_rope_append(const RopeArgs &a, int num_sms, cudaStream_t stream) {
     // Small steps (a decode step's few tokens) take one token per pass, so that
-    // they still spread over many SMs; large ones four.
+    // they still spread over many SMs; large ones kTok.
     const int tpc = a.num_tokens >= num_sms * 8 ? kTok : 1;
     const int chunks = (a.num_tokens + tpc - 1) / tpc;
     const int blocks = std::max(1, std::min(chunks, num_sms * 8));
