@@ -259,9 +259,9 @@ int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool
  *
  * pa_kv_append_fp8: pa_kv_append into fp8 pools (same slot rules and error
  * behaviour).
- * pa_decode_fp8: pa_decode over fp8 pools (head_dim 128 only, else
- * PA_ERR_UNSUPPORTED); same workspace (pa_workspace_size), split-K plan,
- * errors and asynchrony.  q and out stay bf16.
+ * pa_decode_fp8: pa_decode over fp8 pools (head_dim 64 or 128); same
+ * workspace (pa_workspace_size), split-K plan, errors and asynchrony.  q and
+ * out stay bf16.
  */
 int pa_kv_append_fp8(const pa_shape_t *shape, const void *k_new, const void *v_new,
                      const int32_t *slot_mapping, int num_tokens, const float *k_scale,

@@ -58,9 +58,13 @@ constexpr int kQLane = 31;  // the producer lane that loads the items' query row
 template <int D, int BS, bool FP8, bool BIG_G>
 struct DecodeCfg {
     static constexpr int kEB = FP8 ? 1 : 2;                // bytes per pool element
-    static constexpr int kBoxCols = 128 / kEB;             // elements per 128-byte TMA box row
-    static constexpr int kHalves = D / kBoxCols;           // TMA boxes per row
-    static constexpr int kHalfBytes = BS * 128;            // one box: BS rows x 128 B
+    // fp8 rows of d = 64 are 64 bytes: two tokens share one 128-byte TMA row
+    // (token t in row t / 2, bytes 64 (t % 2) ..), so the boxes keep the
+    // 128-byte swizzle; the pool is viewed as rows of 128 bytes.
+    static constexpr bool kPacked = FP8 && D == 64;
+    static constexpr int kBoxCols = kPacked ? 128 : 128 / kEB;  // elements per 128-byte TMA box row
+    static constexpr int kHalves = kPacked ? 1 : D / kBoxCols;  // TMA boxes per row
+    static constexpr int kHalfBytes = BS * D * kEB / kHalves;   // one box: BS tokens' share of it
     static constexpr int kKVBytes = kHalves * kHalfBytes;  // K (or V) of one block
     static constexpr int kStageBytes = 2 * kKVBytes;
     // 96 KB of blocks in flight per CTA (64 KB for G > 8, whose larger merge
@@ -70,7 +74,8 @@ struct DecodeCfg {
     // read only by warp st % 4, block after block, so a warp never waits on
     // a stage's barrier more than one phase ahead.
     static constexpr int kRingBudget = BIG_G ? 65536 : 98304;
-    static constexpr int kStages = (kRingBudget / kStageBytes) / kConsumerWarps * kConsumerWarps;
+    static constexpr int kStagesFit = kRingBudget / kStageBytes < 28 ? kRingBudget / kStageBytes : 28;
+    static constexpr int kStages = kStagesFit / kConsumerWarps * kConsumerWarps;
     static constexpr int kKSteps = D / 16;                 // QK^T k-steps
     static constexpr int kNTiles = D / 8;                  // PV n-tiles
     static constexpr int kRingBytes = kStages * kStageBytes;
@@ -406,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
             const int row = (blk * a.num_kv_heads + it.g) * BS;
 #pragma unroll
             for (int hf = 0; hf < C::kHalves; ++hf) {
-                tma_load_2d(sk + hf * C::kHalfBytes, &tm_k, &full[lane], hf * C::kBoxCols, row);
-                tma_load_2d(sv + hf * C::kHalfBytes, &tm_v, &full[lane], hf * C::kBoxCols, row);
+                tma_load_2d(sk + hf * C::kHalfBytes, &tm_k, &full[lane], hf * C::kBoxCols, C::kPacked ? row / 2 : row);
+                tma_load_2d(sv + hf * C::kHalfBytes, &tm_v, &full[lane], hf * C::kBoxCols, C::kPacked ? row / 2 : row);
             }
         }
         // Every block issued is consumed before the consumers leave, unless a
@@ -418,6 +423,16 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
     }
 
     // --------------------------------------------------------- consumers --
+    // Byte offset of 16-byte chunk jj of token t in an fp8 K or V block (the
+    // 128-byte swizzle XORs the chunk with the row's low three bits).
+    auto kv_off = [](int t, int jj) -> uint32_t {
+        if constexpr (C::kPacked) {
+            const int pr = t >> 1;
+            return pr * 128 + (((jj + 4 * (t & 1)) ^ (pr & 7)) << 4);
+        } else {
+            return t * 128 + ((jj ^ (t & 7)) << 4);
+        }
+    };
     const int G = a.group;
     const int r0 = lane >> 2;       // MMA row (query head within the group)
     const int cq = (lane & 3) * 2;  // first of the lane's two columns
@@ -489,11 +504,20 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                 // Rows past the end of the sequence hold stale pool contents; P is
                 // zero there, but 0 * NaN would still poison the accumulator.
                 uint8_t *vz = smem + st * C::kStageBytes + C::kKVBytes;
-                for (int r = valid + (lane >> 3); r < BS; r += 4) {
-#pragma unroll
-                    for (int hf = 0; hf < C::kHalves; ++hf)
-                        *reinterpret_cast<uint4 *>(vz + hf * C::kHalfBytes + r * 128 + (lane & 7) * 16) =
+                if constexpr (C::kPacked) {
+                    // token r: 16-byte chunks c + 4 (r % 2) of row r / 2, swizzled
+                    for (int e = lane; valid + (e >> 2) < BS; e += 32) {
+                        const int r = valid + (e >> 2), pr = r >> 1;
+                        *reinterpret_cast<uint4 *>(vz + pr * 128 + ((((e & 3) + 4 * (r & 1)) ^ (pr & 7)) << 4)) =
                             make_uint4(0u, 0u, 0u, 0u);
+                    }
+                } else {
+                    for (int r = valid + (lane >> 3); r < BS; r += 4) {
+#pragma unroll
+                        for (int hf = 0; hf < C::kHalves; ++hf)
+                            *reinterpret_cast<uint4 *>(vz + hf * C::kHalfBytes + r * 128 + (lane & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 __syncwarp();
             }
@@ -510,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
 #pragma unroll
                     for (int kp = 0; kp < C::kKSteps / 2; ++kp) {
                         const int jj = 2 * kp + (mat & 1);
-                        const uint32_t addr = sk + t * 128 + (((jj ^ (t & 7))) << 4);
+                        const uint32_t addr = sk + kv_off(t, jj);
                         uint32_t b00, b01, b10, b11;  // (keys 0-7, ks), (0-7, ks+1), (8-15, ks), (8-15, ks+1)
                         ldmatrix_x4(addr, b00, b01, b10, b11);
 #pragma unroll
@@ -597,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
 #pragma unroll
                     for (int jp = 0; jp < D / 32; ++jp) {
                         const int jj = 2 * jp + (mat >> 1);
-                        const uint32_t addr = sv + t * 128 + (((jj ^ (t & 7))) << 4);
+                        const uint32_t addr = sv + kv_off(t, jj);
                         uint32_t v0, v1, v2, v3;  // (keys 0-7, chunk 2jp), (8-15, 2jp), (0-7, 2jp+1), (8-15, 2jp+1)
                         ldmatrix_x4_trans(addr, v0, v1, v2, v3);
 #pragma unroll
@@ -897,6 +921,8 @@ cudaError_t launch_decode(const CUtensorMap &tm_q, const CUtensorMap &tm_k, cons
     PA_DEC(64, 32, false)
     PA_DEC(128, 16, true)
     PA_DEC(128, 32, true)
+    PA_DEC(64, 16, true)
+    PA_DEC(64, 32, true)
 #undef PA_DEC
     return cudaErrorInvalidValue;
 }

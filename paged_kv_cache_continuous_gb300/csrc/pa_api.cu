@@ -151,10 +151,12 @@ int make_pool_map(CUtensorMap *m, const void *pool, const pa_shape_t *sh) {
 int make_pool_map_u8(CUtensorMap *m, const void *pool, const pa_shape_t *sh) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    const cuuint64_t dims[2] = {(cuuint64_t)sh->head_dim,
-                                (cuuint64_t)sh->num_blocks * sh->num_kv_heads * sh->block_size};
-    const cuuint64_t strides[1] = {(cuuint64_t)sh->head_dim};
-    const cuuint32_t box[2] = {(cuuint32_t)sh->head_dim, (cuuint32_t)sh->block_size};
+    // Rows of 128 codes: one token's row for d = 128, two tokens' rows for
+    // d = 64 (the decode kernel addresses token t at row t / 2, half t % 2).
+    const int per_row = 128 / sh->head_dim;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)sh->num_blocks * sh->num_kv_heads * sh->block_size / per_row};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)(sh->block_size / per_row)};
     const cuuint32_t es[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -663,7 +665,6 @@ int pa_decode_fp8(const pa_shape_t *shape, const void *q, const void *k_pool, co
     Range range_("pa_decode_fp8");
     int rc = check_shape(shape);
     if (rc) return rc;
-    if (shape->head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "fp8 decode supports head_dim 128");
     if (num_seqs < 0 || max_seq_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
     if (num_seqs == 0) return ok();
     if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 sequences per call");

@@ -32,11 +32,12 @@ def _case(seed, lens, Hq, Hkv, B, d=128):
     return shape, st, kp0, vp0, q
 
 
-@pytest.mark.parametrize("Hq,Hkv,B", [(32, 8, 16), (32, 32, 16), (64, 4, 32), (64, 8, 16), (16, 8, 32), (40, 8, 16),
-                                      (24, 8, 32)])
-def test_fp8_append_and_decode(cuda_lib, Hq, Hkv, B):
+@pytest.mark.parametrize("Hq,Hkv,B,d", [(32, 8, 16, 128), (32, 32, 16, 128), (64, 4, 32, 128), (64, 8, 16, 128),
+                                        (16, 8, 32, 128), (40, 8, 16, 128), (24, 8, 32, 128),
+                                        (32, 8, 16, 64), (32, 32, 32, 64), (64, 4, 16, 64), (24, 8, 16, 64)])
+def test_fp8_append_and_decode(cuda_lib, Hq, Hkv, B, d):
     lens = [1, 15, 16, 17, 255, 700, 2049]
-    shape, st, kp0, vp0, q = _case(Hq + B, lens, Hq, Hkv, B)
+    shape, st, kp0, vp0, q = _case(Hq + B + d, lens, Hq, Hkv, B, d)
     ks, vs = _scales(Hkv, Hq)
     kd, vd = dev(kp0), dev(vp0)
     pa.kv_append_fp8(shape, dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), dev(ks), dev(vs), kd, vd)
@@ -47,13 +48,14 @@ def test_fp8_append_and_decode(cuda_lib, Hq, Hkv, B):
     out = pa.decode_fp8(shape, dev(q), kd, vd, dev(ks), dev(vs), dev(st.block_table), dev(lens_a), max(lens))
     pa.check_device_error()
     ref = oracle.decode_fp8(bits(q), ek, ev, ks, vs, st.block_table, lens_a)
-    assert_close(out, ref, f"fp8 decode Hq={Hq} Hkv={Hkv} B={B}")
+    assert_close(out, ref, f"fp8 decode Hq={Hq} Hkv={Hkv} B={B} d={d}")
 
 
-def test_fp8_decode_split_vs_single(cuda_lib):
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_decode_split_vs_single(cuda_lib, d):
     """Split-K over fp8 pools agrees with one split (merge path)."""
     lens = [3000, 64, 1234]
-    shape, st, kp0, vp0, q = _case(3, lens, 32, 8, 16)
+    shape, st, kp0, vp0, q = _case(3, lens, 32, 8, 16, d)
     ks, vs = _scales(8, 4)
     kd, vd = dev(kp0), dev(vp0)
     pa.kv_append_fp8(shape, dev(st.k_new), dev(st.v_new), dev(st.slot_mapping), dev(ks), dev(vs), kd, vd)
