@@ -635,9 +635,11 @@ def measure_long_context(pa, wl, dev, hbm_peak, iters):
 def measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, iters):
     """The mixed continuous-batching step: 120 decode sequences (context
     U[1,2048]) + 8 prompts U[64,1024] (sum <= 4096), Hq 32 / Hkv 8, d 128,
-    B 16, through one pa_mixed_step (append, then decode and prefill on two
-    streams); decode and prefill alone beside it.  L2 flushed before each
-    launch.  frac: the step's lower bound with decode (and append) on HBM
+    B 16, through one pa_mixed_step_split (append, then decode and prefill
+    on two streams, the prefill on the CTA pairs pa_mixed_prefill_pairs
+    plans from the host lengths, the decode on the other SMs); the
+    unpartitioned pa_mixed_step, decode and prefill alone beside it.  L2
+    flushed before each launch.  frac: the step's lower bound with decode (and append) on HBM
     and prefill on the tensor cores perfectly overlapped, over its time."""
     shape, kp, vp, st = wl.mixed(pool_device=dev)
     tod = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev) if isinstance(x, np.ndarray) else x.to(dev)
@@ -647,8 +649,13 @@ def measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, iters):
     ws = pa.workspace(shape, nd, st.max_seq_len, dev)
     out = torch.empty_like(q)
     flush = l2_flush_buffer(dev)
+    rows_h = np.diff(st.q_start_loc)[nd:]
+    pairs = pa.mixed_prefill_pairs(shape, st.seq_lens[:nd], rows_h, st.seq_lens[nd:] - rows_h)
     t_step = time_each(dev, lambda: pa.mixed_step(shape, q, kn, vn, qs, lens, slots, bt, nd, st.max_seq_len,
-                                                  st.max_q_len, kp, vp, out=out, ws=ws), iters, flush)
+                                                  st.max_q_len, kp, vp, out=out, ws=ws, prefill_pairs=pairs),
+                       iters, flush)
+    t_shared = time_each(dev, lambda: pa.mixed_step(shape, q, kn, vn, qs, lens, slots, bt, nd, st.max_seq_len,
+                                                    st.max_q_len, kp, vp, out=out, ws=ws), iters, flush)
     dmax = int(st.seq_lens[:nd].max())
     qd, btd, lensd = q[:nd], bt[:nd].contiguous(), lens[:nd].contiguous()
     outd = torch.empty_like(qd)
@@ -671,7 +678,8 @@ def measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, iters):
     del kp, vp
     return {"workload": "120 decode (context U[1,2048]) + 8 prompts U[64,1024] (sum <= 4096), Hq 32 / Hkv 8, "
                         "d 128, B 16", "prompts": n,
-            "step_ms": round(t_step * 1e3, 5), "decode_alone_ms": round(t_dec * 1e3, 5),
+            "step_ms": round(t_step * 1e3, 5), "prefill_pairs": pairs,
+            "step_ms_unpartitioned": round(t_shared * 1e3, 5), "decode_alone_ms": round(t_dec * 1e3, 5),
             "prefill_alone_ms": round(t_pre * 1e3, 5),
             "decode_bytes": nb["decode"], "append_bytes": append_b, "prefill_flops": fl,
             "decode_alone_GBps": round(nb["decode"] / t_dec / 1e9, 1),
@@ -685,8 +693,10 @@ def measure_mixed_step(pa, wl, dev, hbm_peak, bf16_peak, iters):
 def measure_churn(pa, wl, dev, hbm_peak, bf16_peak, warmup):
     """Fragmented serving stress: 512 sequences (log-uniform context in
     [1, 8192]), Hq 32 / Hkv 8, d 128, B 32, 64 consecutive pa_mixed_step
-    calls; after every step a seeded 10 % finish and their blocks are reused
-    by as many prompts U[16,512], prefilled in the next step.  The index trace
+    calls (pa_mixed_step_split, each step's prefill pairs planned from its
+    host lengths; the unpartitioned pa_mixed_step timed beside it); after
+    every step a seeded 10 % finish and their blocks are reused by as many
+    prompts U[16,512], prefilled in the next step.  The index trace
     (lengths, tables, slots) is the one the parity test checks; the rows are
     drawn on the device.  Each step timed with CUDA events; the pools (2.3 GB)
     exceed L2."""
@@ -706,28 +716,36 @@ def measure_churn(pa, wl, dev, hbm_peak, bf16_peak, warmup):
     for st in steps:
         T, nd = int(st.q_start_loc[-1]), st.num_decode
         rows_n = np.diff(st.q_start_loc)
+        pairs = pa.mixed_prefill_pairs(shape, st.seq_lens[:nd], rows_n[nd:], st.seq_lens[nd:] - rows_n[nd:])
         dev_steps.append((T, nd, tod(st.q_start_loc), tod(st.seq_lens), tod(st.slot_mapping), tod(st.block_table),
-                          int(st.seq_lens.max()), int(rows_n[nd:].max()) if len(rows_n) > nd else 1))
+                          int(st.seq_lens.max()), int(rows_n[nd:].max()) if len(rows_n) > nd else 1, pairs))
         bytes_dec.append(T * shape.num_kv_heads * shape.head_dim * 8 + 4 * T)  # + the decode's, below
         n = rows_n[nd:].tolist()
         flops_pre.append(causal_flops(n, [0] * len(n), shape.num_q_heads, shape.head_dim))
         rows_pre.append(int(sum(n)))
 
-    def run(i):
-        T, nd, qs, lens, slots, bt, ml, mq = dev_steps[i]
-        pa.mixed_step(shape, qb[:T], kb[:T], vb[:T], qs, lens, slots, bt, nd, ml, mq, kp, vp, out=outb[:T], ws=ws)
+    def run(i, split=True):
+        T, nd, qs, lens, slots, bt, ml, mq, pairs = dev_steps[i]
+        pa.mixed_step(shape, qb[:T], kb[:T], vb[:T], qs, lens, slots, bt, nd, ml, mq, kp, vp, out=outb[:T], ws=ws,
+                      prefill_pairs=pairs if split else None)
 
-    for i in range(max(3, warmup)):
-        run(i % len(dev_steps))
-    torch.cuda.synchronize(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dev_steps]
-    for i in range(len(dev_steps)):
-        ev[i][0].record()
-        run(i)
-        ev[i][1].record()
-    torch.cuda.synchronize(dev)
-    pa.check_device_error()
-    t = np.array([a.elapsed_time(b) for a, b in ev]) / 1e3
+    def timed(split):
+        for i in range(max(3, warmup)):
+            run(i % len(dev_steps), split)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dev_steps]
+        for i in range(len(dev_steps)):
+            ev[i][0].record()
+            run(i, split)
+            ev[i][1].record()
+        torch.cuda.synchronize(dev)
+        pa.check_device_error()
+        return np.array([a.elapsed_time(b) for a, b in ev]) / 1e3
+
+    # The rows each step appends are the same rows to the same slots every
+    # pass, so the unpartitioned pass sees the same pools.
+    t_shared = timed(False)
+    t = timed(True)
     # Accounting pass (untimed): each step again, then the split its plan
     # launch took, for the decode's algorithmic bytes (the rows appended again
     # are the same rows to the same slots).
@@ -743,6 +761,8 @@ def measure_churn(pa, wl, dev, hbm_peak, bf16_peak, warmup):
     return {"workload": "512 seqs, log-uniform context [1,8192], Hq 32 / Hkv 8, d 128, B 32, 64 steps, 10 % "
                         "replaced per step by prompts U[16,512]",
             "steps": len(t), "step_ms_mean": round(float(t.mean()) * 1e3, 5),
+            "step_ms_mean_unpartitioned": round(float(t_shared.mean()) * 1e3, 5),
+            "prefill_pairs_mean": round(float(np.mean([s[8] for s in dev_steps])), 1),
             "step_ms_p10_p90": [round(float(np.percentile(t, 10)) * 1e3, 5), round(float(np.percentile(t, 90)) * 1e3, 5)],
             "decode_append_GB_per_step": round(float(np.mean(bytes_dec)) / 1e9, 4),
             "prefill_rows_per_step": round(float(np.mean(rows_pre)), 1),

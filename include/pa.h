@@ -217,6 +217,49 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
                   void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * pa_mixed_step with the GPU divided between its two halves (no counterpart
+ * in the pages, which leave the placement of a mixed batch's work to the
+ * hardware).  The prefill runs on prefill_pairs CTA pairs (2 * prefill_pairs
+ * SMs) and the decode on the SMs left over, so both start at once and neither
+ * waits for the other to drain.  prefill_pairs == 0 is exactly pa_mixed_step
+ * (both halves spread over the whole GPU, the prefill placed first).  The
+ * split applies only when both halves have work, the prefill runs the
+ * tensor-core pair kernel (head_dim 128) and 2 * prefill_pairs is below the
+ * device's SM count; otherwise the step runs as pa_mixed_step.  The appended
+ * pools and the prefill rows are bit for bit pa_mixed_step's (a prefill work
+ * unit is summed the same way on any pair); the decode rows agree within the
+ * decode's tolerance, since its split-K factor is chosen for the SMs it gets.
+ * A negative count is PA_ERR_INVALID_ARG.  pa_mixed_prefill_pairs gives a
+ * count for a step.
+ */
+int pa_mixed_step_split(const pa_shape_t *shape, const void *q, const void *k_new,
+                        const void *v_new, const int32_t *q_start_loc,
+                        const int32_t *seq_lens, const int32_t *slot_mapping,
+                        const int32_t *block_table, int max_blocks_per_seq,
+                        int num_seqs, int num_decode, int num_tokens,
+                        int max_seq_len, int max_q_len, void *k_pool,
+                        void *v_pool, void *out, void *workspace,
+                        size_t ws_bytes, void *stream, int prefill_pairs);
+
+/*
+ * The prefill pair count for pa_mixed_step_split, chosen from host-known
+ * lengths so that the two halves take about the same time: decode_lens
+ * [num_decode] are the decode sequences' lengths after the append,
+ * prompt_rows [num_prompts] the new rows of each prompt and prefix_lens
+ * [num_prompts] (NULL = 0) the tokens already cached before them.  The cost
+ * model (measured on GB300): a prefill work unit costs about 3.6 us plus
+ * 1.74 us per 128-key tile on one CTA pair; the decode streams about 45 GB/s
+ * of K/V per SM.  num_sms <= 0 takes the current device's SM count (and then
+ * needs a device); a positive value is used as given (no device needed).
+ * Writes 0 to *pairs (no split) when either half is empty or head_dim is not
+ * 128, else a count in [1, num_sms / 2 - 1].  All arrays are host memory.
+ */
+int pa_mixed_prefill_pairs(const pa_shape_t *shape, const int32_t *decode_lens,
+                           int num_decode, const int32_t *prompt_rows,
+                           const int32_t *prefix_lens, int num_prompts,
+                           int num_sms, int *pairs);
+
+/*
  * Decode without a caller workspace (no counterpart in the pages: an addition
  * for callers that cannot allocate device memory, e.g. code running inside a
  * pre-planned serving loop whose memory is fixed at start-up, or a host that

@@ -28,7 +28,8 @@ ERR_TIMEOUT = 7
 # Every symbol the two headers declare (checked by the tests).
 EXPORTS = [
     "pa_version", "pa_workspace_size", "pa_decode_plan", "pa_kv_append", "pa_decode", "pa_decode_append",
-    "pa_decode_noalloc", "pa_prefill", "pa_mixed_step", "pa_copy_blocks", "pa_rope_append",
+    "pa_decode_noalloc", "pa_prefill", "pa_mixed_step", "pa_mixed_step_split", "pa_mixed_prefill_pairs",
+    "pa_copy_blocks", "pa_rope_append",
     "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_validation", "pa_check_device_error", "pa_last_error",
     "pa_set_decode_split", "pa_set_prefill_pairs",
     "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_ensure", "pa_alloc_release",
@@ -86,6 +87,8 @@ def load():
         "pa_decode_append": ([SP, P, P, P, P, P, P, P, I, P, I, I, P, P, S, P], I),
         "pa_prefill": ([SP, P, P, P, P, P, P, I, I, I, I, P, P], I),
         "pa_mixed_step": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P], I),
+        "pa_mixed_step_split": ([SP, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, S, P, I], I),
+        "pa_mixed_prefill_pairs": ([SP, P, I, P, P, I, I, ctypes.POINTER(I)], I),
         "pa_copy_blocks": ([SP, P, P, I, P, P, I, P, P, I, P], I),
         "pa_rope_append": ([SP, P, P, P, P, P, I, ctypes.c_float, P, P, P, P], I),
         "pa_kv_append_fp8": ([SP, P, P, P, I, P, P, P, P, P], I),
@@ -327,20 +330,40 @@ def prefill(shape, q, k, v, cu_seqlens, max_q_len: int, prefix_lens=None, block_
 
 def mixed_step(shape, q, k_new, v_new, q_start_loc, seq_lens, slot_mapping, block_table,
                num_decode: int, max_seq_len: int, max_q_len: int, k_pool, v_pool, out=None,
-               ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+               ws: torch.Tensor | None = None, stream=None, prefill_pairs: int | None = None) -> torch.Tensor:
+    """pa_mixed_step, or pa_mixed_step_split when prefill_pairs is given."""
     S = int(seq_lens.shape[0])
     if out is None:
         out = torch.empty_like(q)
     if ws is None:
         ws = workspace(shape, max(num_decode, 1), max_seq_len, q.device)
-    _check(load().pa_mixed_step(ctypes.byref(_shape(shape)), _bf16(q, "q"), _bf16(k_new, "k_new"),
-                                _bf16(v_new, "v_new"), _i32(q_start_loc, "q_start_loc"),
-                                _i32(seq_lens, "seq_lens"), _i32(slot_mapping, "slot_mapping"),
-                                _i32(block_table, "block_table"), int(block_table.shape[1]), S,
-                                int(num_decode), int(q.shape[0]), int(max_seq_len), int(max_q_len),
-                                _bf16(k_pool, "k_pool"), _bf16(v_pool, "v_pool"), _bf16(out, "out"),
-                                _ptr(ws), ws.numel(), _stream(stream)))
+    args = (ctypes.byref(_shape(shape)), _bf16(q, "q"), _bf16(k_new, "k_new"),
+            _bf16(v_new, "v_new"), _i32(q_start_loc, "q_start_loc"),
+            _i32(seq_lens, "seq_lens"), _i32(slot_mapping, "slot_mapping"),
+            _i32(block_table, "block_table"), int(block_table.shape[1]), S,
+            int(num_decode), int(q.shape[0]), int(max_seq_len), int(max_q_len),
+            _bf16(k_pool, "k_pool"), _bf16(v_pool, "v_pool"), _bf16(out, "out"),
+            _ptr(ws), ws.numel(), _stream(stream))
+    if prefill_pairs is None:
+        _check(load().pa_mixed_step(*args))
+    else:
+        _check(load().pa_mixed_step_split(*args, int(prefill_pairs)))
     return out
+
+
+def mixed_prefill_pairs(shape, decode_lens, prompt_rows, prefix_lens=None, num_sms: int = 0) -> int:
+    """Prefill CTA pairs for pa_mixed_step_split from host lengths (sequences of ints)."""
+    d = np.ascontiguousarray(np.asarray(decode_lens, dtype=np.int32).reshape(-1))
+    r = np.ascontiguousarray(np.asarray(prompt_rows, dtype=np.int32).reshape(-1))
+    p = None if prefix_lens is None else np.ascontiguousarray(np.asarray(prefix_lens, dtype=np.int32).reshape(-1))
+    if p is not None and p.shape[0] != r.shape[0]:
+        raise ValueError("prefix_lens and prompt_rows differ in length")
+    out = ctypes.c_int(0)
+    _check(load().pa_mixed_prefill_pairs(ctypes.byref(_shape(shape)), d.ctypes.data if d.size else None,
+                                         int(d.size), r.ctypes.data if r.size else None,
+                                         None if p is None or not p.size else p.ctypes.data, int(r.size),
+                                         int(num_sms), ctypes.byref(out)))
+    return out.value
 
 
 def set_validation(on: bool):

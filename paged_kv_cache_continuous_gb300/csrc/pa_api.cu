@@ -222,14 +222,15 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
               int max_seq_len, void *out, void *ws, size_t ws_bytes, cudaStream_t st, DevState *d,
               int check_first, const float *k_scale = nullptr, const float *v_scale = nullptr,
               int split_planned = 0, const void *k_new = nullptr, const void *v_new = nullptr,
-              const int32_t *slot_mapping = nullptr) {
+              const int32_t *slot_mapping = nullptr, int decode_sms = 0) {
     const bool fp8 = k_scale != nullptr;
+    const int sms = decode_sms > 0 ? std::min(decode_sms, d->num_sms) : d->num_sms;  // SMs the decode may fill
     // split_planned > 0: the caller has already planned the split (and sized
     // its scratch from it); the override is not read a second time.
     const int override_tokens = g_split_override.load();
     const int split = split_planned > 0 ? split_planned
                                         : decode_split_tokens(num_seqs, sh->num_kv_heads, max_seq_len,
-                                                              sh->block_size, d->num_sms, override_tokens);
+                                                              sh->block_size, sms, override_tokens);
     const int max_splits = decode_max_splits(max_seq_len, split);
     const size_t need = decode_workspace_bytes(num_seqs, sh->num_q_heads, sh->num_kv_heads, sh->head_dim,
                                                max_splits);
@@ -280,7 +281,7 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
         a.v_pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_pool));
         a.num_slots = (long long)sh->num_blocks * sh->block_size;
     }
-    cudaError_t e = launch_decode(tq, tk, tv, a, sh->head_dim, sh->block_size, d->num_sms, st, fp8);
+    cudaError_t e = launch_decode(tq, tk, tv, a, sh->head_dim, sh->block_size, sms, st, fp8);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return PA_OK;
 }
@@ -288,7 +289,7 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
 int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v, const int32_t *cu,
                const int32_t *prefix_lens, const int32_t *seq_lens, const int32_t *block_table,
                int max_blocks, int num_seqs, int num_tokens, int max_q_len, void *out, cudaStream_t st,
-               DevState *d, int check_first) {
+               DevState *d, int check_first, int pairs = 0) {
     CUtensorMap tq, tk, tv;
     int rc = make_rows_map(&tq, q, sh->head_dim, sh->num_q_heads, num_tokens);
     if (rc) return rc;
@@ -320,7 +321,7 @@ int do_prefill(const pa_shape_t *sh, const void *q, const void *k, const void *v
     a.check_err_first = check_first;
     a.scale_log2 = scale_log2(sh);
     {
-        const int ov = g_pairs_override.load();
+        const int ov = pairs > 0 ? pairs : g_pairs_override.load();
         a.num_sms = ov > 0 ? std::min(2 * ov, d->num_sms) : d->num_sms;
     }
     cudaError_t e;
@@ -787,13 +788,47 @@ int pa_prefill(const pa_shape_t *shape, const void *q, const void *k, const void
     return ok();
 }
 
-int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
-                  const int32_t *q_start_loc, const int32_t *seq_lens, const int32_t *slot_mapping,
-                  const int32_t *block_table, int max_blocks_per_seq, int num_seqs, int num_decode,
-                  int num_tokens, int max_seq_len, int max_q_len, void *k_pool, void *v_pool, void *out,
-                  void *workspace, size_t ws_bytes, void *stream) {
-    Range range_("pa_mixed_step");
+// Prefill CTA pairs for a mixed step whose halves run side by side: the
+// count that gives both the same time under a cost model measured on GB300.
+// The prefill pair kernel costs about 1.74 us per 128-key tile-step of a work
+// unit plus 3.6 us per unit, on one CTA pair (a fit over uniform prompt
+// sets); the decode streams about 45 GB/s of K/V per SM.  With A pair-us of
+// prefill work and B SM-us of decode work, A / P = B / (S - 2 P) at
+// P = S A / (B + 2 A).  0 (no split) when a half is empty or head_dim is not
+// 128 (only the pair kernel takes a pair count).
+static int mixed_prefill_pairs(const pa_shape_t *sh, const int32_t *decode_lens, int nd, const int32_t *rows,
+                               const int32_t *prefix, int np, int num_sms) {
+    if (nd <= 0 || np <= 0 || sh->head_dim != 128 || num_sms < 6) return 0;
+    const int group = sh->num_q_heads / sh->num_kv_heads;
+    const int per_unit = group % 4 == 0 ? 1 : (group % 2 == 0 ? 2 : 4);   // row tiles of a head in one unit
+    const int ny = sh->num_q_heads / (group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1));  // units per level
+    double units = 0.0, steps = 0.0;
+    for (int i = 0; i < np; ++i) {
+        const long long n = rows[i], p0 = prefix ? std::max(0, prefix[i]) : 0;
+        if (n <= 0) continue;
+        const long long levels = ((n + 127) / 128 + per_unit - 1) / per_unit;
+        for (long long px = 0; px < levels; ++px) {
+            const long long kv_end = p0 + std::min(n, (px + 1) * per_unit * 128);
+            units += ny;
+            steps += (double)ny * ((kv_end + 127) / 128);
+        }
+    }
+    double bytes = 0.0;
+    for (int i = 0; i < nd; ++i) bytes += (double)std::max(0, decode_lens[i]) * sh->num_kv_heads * sh->head_dim * 4.0;
+    const double a = 3.6 * units + 1.74 * steps;  // pair-us
+    const double b = bytes / 45e3;                // SM-us at 45 GB/s per SM
+    if (a <= 0.0 || b <= 0.0) return 0;
+    const int p = (int)std::lround(num_sms * a / (b + 2.0 * a));
+    return std::max(1, std::min(p, num_sms / 2 - 1));
+}
+
+static int mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                      const int32_t *q_start_loc, const int32_t *seq_lens, const int32_t *slot_mapping,
+                      const int32_t *block_table, int max_blocks_per_seq, int num_seqs, int num_decode,
+                      int num_tokens, int max_seq_len, int max_q_len, void *k_pool, void *v_pool, void *out,
+                      void *workspace, size_t ws_bytes, void *stream, int prefill_pairs) {
     int rc = check_shape(shape);
+    if (prefill_pairs < 0) return fail(PA_ERR_INVALID_ARG, "prefill_pairs < 0");
     if (rc) return rc;
     if (num_seqs < 0 || num_decode < 0 || num_decode > num_seqs || num_tokens < 0 || max_seq_len < 0 ||
         max_q_len < 0)
@@ -844,15 +879,20 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
                          static_cast<const __nv_bfloat16 *>(v_new) + (size_t)num_decode * row,
                          slot_mapping + num_decode, prompt_rows, k_pool, v_pool, s, d, val);
     };
+    // prefill_pairs > 0 (and fewer than the SMs hold): the prefill runs on
+    // that many CTA pairs and the decode fills the other SMs only, side by side.
+    const bool split_sms = has_prefill && num_decode > 0 && prefill_pairs > 0 && shape->head_dim == 128 &&
+                           2 * prefill_pairs < d->num_sms;
     auto prefill_on = [&](cudaStream_t s) {
         return do_prefill(shape, q, k_pool, v_pool, q_start_loc + num_decode, nullptr, seq_lens + num_decode,
                           block_table + (size_t)num_decode * max_blocks_per_seq, max_blocks_per_seq, np,
-                          num_tokens, max_q_len, out, s, d, val);
+                          num_tokens, max_q_len, out, s, d, val, split_sms ? prefill_pairs : 0);
     };
     auto decode_on = [&](cudaStream_t s) {
+        const int dsms = split_sms ? d->num_sms - 2 * prefill_pairs : 0;
         return do_decode(shape, q, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, num_decode,
                          max_seq_len, out, workspace, ws_bytes, s, d, val, nullptr, nullptr, 0, k_new, v_new,
-                         slot_mapping);
+                         slot_mapping, dsms);
     };
     if (num_decode > 0 && has_prefill) {
         std::lock_guard<std::mutex> lk(g_side_mu);
@@ -883,6 +923,45 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, con
     if (num_decode > 0 && (rc = decode_on(st))) return rc;
     if ((rc = append_prompts(st))) return rc;
     if (has_prefill && (rc = prefill_on(st))) return rc;
+    return ok();
+}
+
+int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                  const int32_t *q_start_loc, const int32_t *seq_lens, const int32_t *slot_mapping,
+                  const int32_t *block_table, int max_blocks_per_seq, int num_seqs, int num_decode,
+                  int num_tokens, int max_seq_len, int max_q_len, void *k_pool, void *v_pool, void *out,
+                  void *workspace, size_t ws_bytes, void *stream) {
+    Range range_("pa_mixed_step");
+    return mixed_step(shape, q, k_new, v_new, q_start_loc, seq_lens, slot_mapping, block_table, max_blocks_per_seq,
+                      num_seqs, num_decode, num_tokens, max_seq_len, max_q_len, k_pool, v_pool, out, workspace,
+                      ws_bytes, stream, 0);
+}
+
+int pa_mixed_step_split(const pa_shape_t *shape, const void *q, const void *k_new, const void *v_new,
+                        const int32_t *q_start_loc, const int32_t *seq_lens, const int32_t *slot_mapping,
+                        const int32_t *block_table, int max_blocks_per_seq, int num_seqs, int num_decode,
+                        int num_tokens, int max_seq_len, int max_q_len, void *k_pool, void *v_pool, void *out,
+                        void *workspace, size_t ws_bytes, void *stream, int prefill_pairs) {
+    Range range_("pa_mixed_step_split");
+    return mixed_step(shape, q, k_new, v_new, q_start_loc, seq_lens, slot_mapping, block_table, max_blocks_per_seq,
+                      num_seqs, num_decode, num_tokens, max_seq_len, max_q_len, k_pool, v_pool, out, workspace,
+                      ws_bytes, stream, prefill_pairs);
+}
+
+int pa_mixed_prefill_pairs(const pa_shape_t *shape, const int32_t *decode_lens, int num_decode,
+                           const int32_t *prompt_rows, const int32_t *prefix_lens, int num_prompts, int num_sms,
+                           int *pairs) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!pairs || num_decode < 0 || num_prompts < 0 || (num_decode > 0 && !decode_lens) ||
+        (num_prompts > 0 && !prompt_rows))
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer or negative count");
+    if (num_sms <= 0) {
+        DevState *d;
+        if ((rc = dev_state(&d))) return rc;
+        num_sms = d->num_sms;
+    }
+    *pairs = mixed_prefill_pairs(shape, decode_lens, num_decode, prompt_rows, prefix_lens, num_prompts, num_sms);
     return ok();
 }
 

@@ -1,5 +1,6 @@
 """Closed-loop continuous batching: the host scheduler (include/pa_sched.h)
-plans each step, one pa_mixed_step runs it on the GPU, the scheduler commits
+plans each step, one pa_mixed_step_split runs it on the GPU (prefill and
+decode side by side on a planned division of the SMs), the scheduler commits
 it.  Mock mode: there is no model, so each step's queries, keys and values
 are seeded random bf16 rows (the attention path sees the shapes, ragged
 lengths and pool traffic of a served batch); requests arrive from a
@@ -35,6 +36,7 @@ class ServingLoop:
         self.last = None  # the last step's inputs (host numpy / device tensors), for checking
         self.gpu_events = []  # (start, end) CUDA events around each step's pa_mixed_step, if timed
         self.time_gpu = False
+        self.partition = True  # pa_mixed_step_split on the planned pair count (False: pa_mixed_step)
 
     def submit(self, request_id: int, input_tokens: int, max_new_tokens: int):
         self.sched.submit(request_id, input_tokens, max_new_tokens)
@@ -64,7 +66,12 @@ class ServingLoop:
         if self.time_gpu:
             ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             ev[0].record()
-        out = pa.mixed_step(sh, q, kn, vn, qs, lens, slots, bt, nd, max_len, max_q, self.kp, self.vp)
+        # The GPU's SMs are divided between the step's prefill and decode by
+        # the cost model, from the lengths the plan already holds on the host.
+        lens_h = plan["seq_lens"]
+        pairs = pa.mixed_prefill_pairs(sh, lens_h[:nd], rows[nd:], lens_h[nd:] - rows[nd:]) if self.partition else None
+        out = pa.mixed_step(sh, q, kn, vn, qs, lens, slots, bt, nd, max_len, max_q, self.kp, self.vp,
+                            prefill_pairs=pairs)
         if self.time_gpu:
             ev[1].record()
             self.gpu_events.append(ev)

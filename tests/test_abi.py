@@ -129,3 +129,56 @@ def test_workspace_size(lib):
     assert lib.pa_set_prefill_pairs(3) == 0
     assert lib.pa_set_prefill_pairs(0) == 0
     assert lib.pa_set_prefill_pairs(-1) == binding.ERR_INVALID_ARG
+
+
+def _pairs(lib, sh, dec, rows, prefix=None, sms=152):
+    arr = lambda xs: (ctypes.c_int32 * max(1, len(xs)))(*xs)
+    out = ctypes.c_int(-7)
+    rc = lib.pa_mixed_prefill_pairs(ctypes.byref(sh), arr(dec), len(dec), arr(rows),
+                                    None if prefix is None else arr(prefix), len(rows), sms, ctypes.byref(out))
+    return rc, out.value
+
+
+def test_mixed_prefill_pairs_planner(lib):
+    """The SM partition of a mixed step: 0 when a half is empty or head_dim is
+    64, else the balance point of the cost model, inside [1, S/2 - 1]."""
+    sh = binding.PaShape(32, 8, 128, 16, 100, 0.0)
+    assert _pairs(lib, sh, [], [512]) == (0, 0)
+    assert _pairs(lib, sh, [1000], []) == (0, 0)
+    assert _pairs(lib, binding.PaShape(32, 8, 64, 16, 100, 0.0), [1000], [512]) == (0, 0)
+    # One 128-row prompt: 8 head groups of 4 (Hq 32 / Hkv 8), one tile each:
+    # A = 8 * 3.6 + 8 * 1.74 pair-us.  One decode of L tokens moves
+    # L * 8 * 128 * 4 bytes at 45 GB/s per SM.
+    for L in (2000, 20000, 200000):
+        a = 8 * 3.6 + 8 * 1.74
+        b = L * 8 * 128 * 4 / 45e3
+        want = max(1, min(round(152 * a / (b + 2 * a)), 75))
+        assert _pairs(lib, sh, [L], [128]) == (0, want)
+    # more decode work -> fewer pairs; more prefill work (rows, prefix) -> more
+    base = _pairs(lib, sh, [1500] * 64, [256, 512])[1]
+    assert 1 <= base <= 75
+    assert _pairs(lib, sh, [1500] * 128, [256, 512])[1] < base
+    assert _pairs(lib, sh, [1500] * 64, [256, 512, 1024])[1] > base
+    assert _pairs(lib, sh, [1500] * 64, [256, 512], [4096, 4096])[1] > base
+    # clamps: a tiny decode leaves the prefill all but one pair, and a huge
+    # one still gives the prefill a pair
+    assert _pairs(lib, sh, [1], [4096] * 8)[1] == 75
+    assert _pairs(lib, sh, [10 ** 6] * 64, [16])[1] == 1
+    assert _pairs(lib, sh, [1], [4096] * 8, sms=100)[1] == 49
+    # group 2 (two row tiles a unit) and group 1 (four)
+    for hq, hkv in ((16, 8), (8, 8)):
+        assert 1 <= _pairs(lib, binding.PaShape(hq, hkv, 128, 16, 100, 0.0), [3000] * 32, [700, 300])[1] <= 75
+    bad = ctypes.c_int()
+    assert lib.pa_mixed_prefill_pairs(ctypes.byref(sh), None, 1, None, None, 0, 152,
+                                      ctypes.byref(bad)) == binding.ERR_INVALID_ARG
+    assert lib.pa_mixed_prefill_pairs(ctypes.byref(sh), None, 0, None, None, 0, 152, None) == binding.ERR_INVALID_ARG
+    # the split step rejects a negative count before anything else
+    assert lib.pa_mixed_step_split(ctypes.byref(sh), DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, 4, 2, 1, 8,
+                                   64, 8, DUMMY, DUMMY, DUMMY, DUMMY, 0, None, -1) == binding.ERR_INVALID_ARG
+
+
+def test_mixed_prefill_pairs_binding(lib):
+    shape = binding.PaShape(32, 8, 128, 16, 100, 0.0)
+    n = binding.mixed_prefill_pairs(shape, [1500] * 64, [256, 512], num_sms=152)
+    assert n == _pairs(lib, shape, [1500] * 64, [256, 512])[1]
+    assert binding.mixed_prefill_pairs(shape, [], [256], num_sms=152) == 0

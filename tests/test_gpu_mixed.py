@@ -115,3 +115,50 @@ def test_churn_64_steps(cuda_lib):
         _sampled_step_check(shape, st, out, kd, vd, rng, f"churn step {step}", host_pool=(kh, vh))
         if step in (0, 31, ch.steps - 1):
             assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh), f"pool differs at {step}"
+
+
+@pytest.mark.parametrize("pairs", [1, 7, "planned", 75, 76, 1000])
+def test_mixed_split_small(cuda_lib, pairs):
+    """pa_mixed_step_split at several prefill pair counts (76 and above: no
+    room left for the decode, so the step runs unsplit): pools bit-exact,
+    every output row within tolerance of the oracle, prefill rows bit-exact
+    with the unsplit step's."""
+    shape, kp, vp, st = wl.mixed(seed=34, num_decode=24, num_prompts=5, prompt_range=(1, 400),
+                                 prefill_budget=1200, max_context=900)
+    nd = st.num_decode
+    if pairs == "planned":
+        rows = np.diff(st.q_start_loc)[nd:]
+        pairs = pa.mixed_prefill_pairs(shape, st.seq_lens[:nd], rows, st.seq_lens[nd:] - rows)
+        assert pairs >= 1
+    kd, vd = dev(kp), dev(vp)
+    args = (shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(st.q_start_loc), dev(st.seq_lens),
+            dev(st.slot_mapping), dev(st.block_table), nd, st.max_seq_len, st.max_q_len)
+    out = pa.mixed_step(*args, kd, vd, prefill_pairs=pairs)
+    pa.check_device_error()
+    ref, kh, vh = oracle.mixed_step(bits(st.q), bits(st.k_new), bits(st.v_new), st.q_start_loc, st.seq_lens,
+                                    st.slot_mapping, st.block_table, nd, bits(kp), bits(vp))
+    assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh)
+    assert_close(out, ref, f"mixed split {pairs}")
+    kd2, vd2 = dev(kp), dev(vp)
+    out2 = pa.mixed_step(*args, kd2, vd2)
+    pa.check_device_error()
+    r0 = int(st.q_start_loc[nd])
+    assert torch.equal(out[r0:], out2[r0:]), "prefill rows differ from the unsplit step"
+
+
+def test_mixed_split_full_size_planned(cuda_lib):
+    """The 120-decode + 8-prompt step on the planned partition: pools
+    bit-exact, sampled outputs vs the oracle."""
+    shape, kp, vp, st = wl.mixed()
+    nd = st.num_decode
+    rows = np.diff(st.q_start_loc)[nd:]
+    pairs = pa.mixed_prefill_pairs(shape, st.seq_lens[:nd], rows, st.seq_lens[nd:] - rows)
+    assert 1 <= pairs < torch.cuda.get_device_properties(0).multi_processor_count // 2
+    kd, vd = dev(kp), dev(vp)
+    out = pa.mixed_step(shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(st.q_start_loc), dev(st.seq_lens),
+                        dev(st.slot_mapping), dev(st.block_table), nd, st.max_seq_len, st.max_q_len, kd, vd,
+                        prefill_pairs=pairs)
+    pa.check_device_error()
+    kh, vh = oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, bits(kp), bits(vp))
+    assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh)
+    _sampled_step_check(shape, st, out, kd, vd, np.random.default_rng(6), "mixed split full", host_pool=(kh, vh))
