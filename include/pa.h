@@ -247,9 +247,9 @@ int pa_mixed_step_split(const pa_shape_t *shape, const void *q, const void *k_ne
  * [num_decode] are the decode sequences' lengths after the append,
  * prompt_rows [num_prompts] the new rows of each prompt and prefix_lens
  * [num_prompts] (NULL = 0) the tokens already cached before them.  The cost
- * model (measured on GB300): a prefill work unit costs about 3.6 us plus
- * 1.74 us per 128-key tile on one CTA pair; the decode streams about 45 GB/s
- * of K/V per SM.  num_sms <= 0 takes the current device's SM count (and then
+ * model (fit to timings on GB300): a prefill work unit costs about 1 us plus
+ * 2 us per 128-key tile on one CTA pair; the decode streams about 50 GB/s of
+ * K/V per SM.  num_sms <= 0 takes the current device's SM count (and then
  * needs a device); a positive value is used as given (no device needed).
  * Writes 0 to *pairs (no split) when either half is empty or head_dim is not
  * 128, else a count in [1, num_sms / 2 - 1].  All arrays are host memory.

@@ -790,9 +790,10 @@ int pa_prefill(const pa_shape_t *shape, const void *q, const void *k, const void
 
 // Prefill CTA pairs for a mixed step whose halves run side by side: the
 // count that gives both the same time under a cost model measured on GB300.
-// The prefill pair kernel costs about 1.74 us per 128-key tile-step of a work
-// unit plus 3.6 us per unit, on one CTA pair (a fit over uniform prompt
-// sets); the decode streams about 45 GB/s of K/V per SM.  With A pair-us of
+// The prefill pair kernel costs about 2 us per 128-key tile-step of a work
+// unit plus 1 us per unit, on one CTA pair; the decode streams about 50 GB/s
+// of K/V per SM (a fit to the per-step optimum of a 64-step churn of 512
+// sequences and to a 120-decode + 8-prompt step, each timed at 30 pair counts).  With A pair-us of
 // prefill work and B SM-us of decode work, A / P = B / (S - 2 P) at
 // P = S A / (B + 2 A).  0 (no split) when a half is empty or head_dim is not
 // 128 (only the pair kernel takes a pair count).
@@ -815,8 +816,8 @@ static int mixed_prefill_pairs(const pa_shape_t *sh, const int32_t *decode_lens,
     }
     double bytes = 0.0;
     for (int i = 0; i < nd; ++i) bytes += (double)std::max(0, decode_lens[i]) * sh->num_kv_heads * sh->head_dim * 4.0;
-    const double a = 3.6 * units + 1.74 * steps;  // pair-us
-    const double b = bytes / 45e3;                // SM-us at 45 GB/s per SM
+    const double a = 1.0 * units + 2.0 * steps;  // pair-us
+    const double b = bytes / 50e3;               // SM-us at 50 GB/s per SM
     if (a <= 0.0 || b <= 0.0) return 0;
     const int p = (int)std::lround(num_sms * a / (b + 2.0 * a));
     return std::max(1, std::min(p, num_sms / 2 - 1));

@@ -147,11 +147,11 @@ def test_mixed_prefill_pairs_planner(lib):
     assert _pairs(lib, sh, [1000], []) == (0, 0)
     assert _pairs(lib, binding.PaShape(32, 8, 64, 16, 100, 0.0), [1000], [512]) == (0, 0)
     # One 128-row prompt: 8 head groups of 4 (Hq 32 / Hkv 8), one tile each:
-    # A = 8 * 3.6 + 8 * 1.74 pair-us.  One decode of L tokens moves
-    # L * 8 * 128 * 4 bytes at 45 GB/s per SM.
+    # A = 8 * 1 + 8 * 2 pair-us.  One decode of L tokens moves
+    # L * 8 * 128 * 4 bytes at 50 GB/s per SM.
     for L in (2000, 20000, 200000):
-        a = 8 * 3.6 + 8 * 1.74
-        b = L * 8 * 128 * 4 / 45e3
+        a = 8 * 1.0 + 8 * 2.0
+        b = L * 8 * 128 * 4 / 50e3
         want = max(1, min(round(152 * a / (b + 2 * a)), 75))
         assert _pairs(lib, sh, [L], [128]) == (0, want)
     # more decode work -> fewer pairs; more prefill work (rows, prefix) -> more
