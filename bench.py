@@ -65,6 +65,8 @@ def decode_step_bytes(shape, seq_lens: np.ndarray, split: int, block_size: int) 
     qo = 2 * S * Hq * d * 2
     tables = int(np.ceil(L / block_size).sum()) * 4 + S * 4
     nsplit = np.maximum(1, -(-L // split))
+    # a last split of at most split / 8 tokens joins the one before
+    nsplit = np.where((nsplit > 1) & (L - (nsplit - 1) * split <= split // 8), nsplit - 1, nsplit)
     multi = nsplit > 1
     partials = int((nsplit[multi]).sum()) * Hq * (d + 2) * 4 * 2
     append = S * Hkv * d * 2 * 2 * 2 + S * 4  # read k_new, v_new; write the rows; slots
@@ -220,7 +222,7 @@ def run_ours(args, world, rank, local):
     _, max_splits = pa.decode_plan(shape, st.num_seqs, max_len)
     split = pa.planned_split(ws, shape, st.num_seqs, max_len)  # the split the plan launch took
     nbytes = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
-    launches_per_step = 1 + (1 if max_splits > 1 else 0)
+    launches_per_step = 2  # the plan launch (with the append) and the decode kernel
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -298,7 +300,7 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs larger than L2 (KV pools 2.4 GB > 129 MB); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm",
-                     "kernel": "decode with the append fused (decode_splitk_kernel + decode_merge_kernel)",
+                     "kernel": "decode with the append fused (decode_plan_kernel + decode_splitk_kernel, splits merged in-kernel)",
                      "achieved": round(nbytes["step"] / t_dec / 1e9, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(nbytes["step"] / t_dec / 1e9 / hbm_peak, 4),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy)",
@@ -410,11 +412,44 @@ def measure_prefill(pa, wl, dev, bf16_peak, peak_src, iters):
         res[name] = {"prompts": n if len(n) <= 8 else len(n), "ms": round(t * 1e3, 4),
                      "tflops": round(fl / t / 1e12, 1), "frac": round(fl / t / 1e12 / bf16_peak, 4)}
         del kp, vp
+        # Back to back: the same prompt lengths in four input sets of their
+        # own (fresh pools, queries and outputs: ~86 MB each for 4096 rows, so
+        # four exceed L2 and every launch reads its inputs from DRAM), one
+        # launch after another with no flush between, one event pair around
+        # them all: the rate a stream of prefills runs at, without the
+        # launch latency a lone launch after a flush is timed with.
+        sets = []
+        for j in range(4):
+            shp, kpj, vpj, stj = wl.prefill_only(200 + 10 * j + len(n), n, pool_device=dev)
+            qj = stj.q.to(dev)
+            pa.kv_append(shp, stj.k_new.to(dev), stj.v_new.to(dev), torch.from_numpy(stj.slot_mapping).to(dev),
+                         kpj, vpj)
+            sets.append((shp, qj, kpj, vpj, torch.from_numpy(stj.q_start_loc).to(dev),
+                         torch.from_numpy(stj.block_table).to(dev), torch.empty_like(qj)))
+        for shp, qj, kpj, vpj, cuj, btj, oj in sets:
+            pa.prefill(shp, qj, kpj, vpj, cuj, max(n), block_table=btj, out=oj)
+        torch.cuda.synchronize(dev)
+        n_l = 4 * max(iters // 2, 10)
+        torch.cuda._sleep(int(2e6 + 2e5 * n_l))  # the launches queue up before the GPU reaches them
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for j in range(n_l):
+            shp, qj, kpj, vpj, cuj, btj, oj = sets[j % 4]
+            pa.prefill(shp, qj, kpj, vpj, cuj, max(n), block_table=btj, out=oj)
+        b.record()
+        torch.cuda.synchronize(dev)
+        pa.check_device_error()
+        t2 = a.elapsed_time(b) / 1e3 / n_l
+        res[name]["back_to_back"] = {"ms": round(t2 * 1e3, 4), "tflops": round(fl / t2 / 1e12, 1),
+                                     "frac": round(fl / t2 / 1e12 / bf16_peak, 4), "launches": n_l,
+                                     "l2": "four input sets in turn (inputs larger than L2); no flush"}
+        del sets
     best = max(res.values(), key=lambda r: r["tflops"])
     return {"bound": "tensor", "kernel": "prefill_pair_kernel (tcgen05 cta_group::2, P in TMEM; head_dim 128)", "unit": "TFLOP/s",
             "peak": bf16_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst)",
             "workloads": res, "achieved_best": best["tflops"], "frac_best": best["frac"],
-            "flops_counted": "4*d*Hq per unmasked causal (row, key) pair", "l2": "flushed (256 MB write) before each launch"}
+            "flops_counted": "4*d*Hq per unmasked causal (row, key) pair",
+            "l2": "flushed (256 MB write) before each launch (back_to_back: see its own l2 key)"}
 
 
 def measure_copy(pa, wl, dev, hbm_peak, iters):
@@ -570,7 +605,7 @@ def measure_fp8_decode(pa, wl, dev, hbm_peak, steps):
     split = pa.planned_split(ws, shape, st.num_seqs, st.max_seq_len)
     nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
     fp8_bytes = nb["decode"] - nb["kv"] // 2
-    return {"kernel": "decode_splitk_kernel<128,16,*,fp8> + decode_merge_kernel", "ms": round(t * 1e3, 5),
+    return {"kernel": "decode_splitk_kernel<128,16,*,fp8> (splits merged in-kernel)", "ms": round(t * 1e3, 5),
             "GBps": round(fp8_bytes / t / 1e9, 1), "frac_hbm": round(fp8_bytes / t / 1e9 / hbm_peak, 4),
             "algorithmic_bytes": int(fp8_bytes), "sequences_per_s": round(st.num_seqs / t, 1),
             "l2": "inputs larger than L2 (fp8 pools 1.2 GB)"}
@@ -623,10 +658,12 @@ def measure_long_context(pa, wl, dev, hbm_peak, iters):
     pa.check_device_error()
     split = pa.planned_split(ws, shape, st.num_seqs, st.max_seq_len)
     nsplit = -(-int(st.max_seq_len) // split)
+    if nsplit > 1 and int(st.max_seq_len) - (nsplit - 1) * split <= split // 8:
+        nsplit -= 1
     nb = decode_step_bytes(shape, st.seq_lens, split, shape.block_size)
     del kp, vp
     return {"workload": "32 x 32768 cached tokens (+1), Hq 64 / Hkv 8, d 128, B 16",
-            "kernel": "decode_splitk_kernel + decode_merge_kernel", "split_tokens": split, "splits": nsplit,
+            "kernel": "decode_splitk_kernel (splits merged in-kernel)", "split_tokens": split, "splits": nsplit,
             "decode_ms": round(t_dec * 1e3, 5), "algorithmic_bytes": nb["decode"],
             "GBps": round(nb["decode"] / t_dec / 1e9, 1), "frac_hbm": round(nb["decode"] / t_dec / 1e9 / hbm_peak, 4),
             "append_ms": round(t_app * 1e3, 5), "l2": "inputs larger than L2 (pools 4.7 GB); no flush"}

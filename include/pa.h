@@ -98,8 +98,9 @@ int pa_version(void);
  * pa_mixed_step for batches of at most max_seqs sequences whose lengths
  * (after the step's append) are at most max_seq_len.  The workspace holds the
  * decode plan (the batch's work items, one per sequence, KV head and split,
- * its counters and 8 bytes per sequence) and the split-K partial results
- * (fp32); it is owned by
+ * its counters, 8 bytes per sequence and, when a sequence can split, a merge
+ * count per sequence and KV head) and the split-K partial results (fp32); it
+ * is owned by
  * the caller, its contents need no initialisation, and two calls whose
  * kernels may overlap on the GPU need two workspaces.  Writes *bytes.
  */
@@ -112,13 +113,18 @@ int pa_workspace_size(const pa_shape_t *shape, int max_seqs, int max_seq_len,
  * longest sequence, for num_seqs sequences of at most max_seq_len tokens on
  * the current device (its SM count enters the choice).  This is the finest
  * split the decode uses: its plan launch, which sees the batch's lengths,
- * takes split_tokens * 2^k instead (k <= 5) when that still leaves at least
- * six work items per decode CTA and no item longer than half of a CTA's share
- * of the tokens -- fewer, longer items cost less.  Sequence s then uses
- * ceil(seq_lens[s] / split) splits (1 if it is empty), never more than
- * max_splits; a sequence with one split writes its output directly, the
- * others go through the merge.  With pa_set_decode_split in effect the split
- * is exactly the override.
+ * takes split_tokens * 2^k (k <= 5) instead -- no split at all when even the
+ * longest sequence is at most 3/5 of a decode CTA's share of the batch's KV
+ * blocks, else the largest k that still leaves at least six work items per
+ * decode CTA and no item longer than half of a CTA's share (fewer, longer
+ * items cost less while the CTAs stay evenly loaded).  pa_workspace_size
+ * covers every such choice.  Sequence s then uses
+ * ceil(seq_lens[s] / split) splits (1 if it is empty), one fewer when the
+ * last would hold at most split / 8 tokens (they join the split before),
+ * never more than max_splits; a sequence with one split writes its output directly; for the
+ * others, the split of each (sequence, KV head) that finishes last merges
+ * all of its splits' partials, inside the decode kernel.  With
+ * pa_set_decode_split in effect the split is exactly the override.
  */
 int pa_decode_plan(const pa_shape_t *shape, int num_seqs, int max_seq_len,
                    int *split_tokens, int *max_splits);
@@ -139,8 +145,9 @@ int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new,
  * sequence's seq_lens[s] cached tokens (counted after the step's append),
  * read through block_table.  out [S][Hq][d].  seq_lens[s] == 0 gives zeros.
  * Long contexts are split into chunks (split-K) whose partial softmax states
- * are merged by a second kernel; the split is chosen from max_seq_len, which
- * must bound every seq_lens[s] (a longer sequence sets the device error word).
+ * are merged in the same kernel, by the chunk of each (sequence, KV head)
+ * that finishes last; the split is chosen from max_seq_len, which must bound
+ * every seq_lens[s] (a longer sequence sets the device error word).
  * workspace: at least pa_workspace_size(shape, num_seqs, max_seq_len) bytes.
  */
 int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool,
@@ -274,15 +281,17 @@ int pa_mixed_prefill_pairs(const pa_shape_t *shape, const int32_t *decode_lens,
  *  - A batch whose partials need more than the buffer holds is rejected
  *    with PA_ERR_WORKSPACE before anything is enqueued; use pa_decode then.
  *    The exact need, with max_splits from pa_decode_plan(shape, num_seqs,
- *    max_seq_len), is P + num_seqs * (max_splits * Hkv * 16 + 8) + 16 bytes, where
- *    P = num_seqs * Hq * max_splits * (d + 2) * 4 rounded up to a multiple
- *    of 16 (P = 0 when max_splits is 1).  pa_workspace_size(shape, num_seqs,
+ *    max_seq_len), is P + num_seqs * (max_splits * Hkv * 16 + 8) + 16 + C
+ *    bytes, where P = num_seqs * Hq * max_splits * (d + 2) * 4 rounded up to
+ *    a multiple of 16 and C = num_seqs * Hkv * 4 (P = C = 0 when max_splits
+ *    is 1).  pa_workspace_size(shape, num_seqs,
  *    max_seq_len) is an upper bound of that need (it assumes the shortest
  *    split), so a batch with pa_workspace_size <= PA_NOALLOC_SCRATCH_BYTES is
  *    always accepted, and larger ones often are.
  *  - All calls share the one buffer and nothing in it needs clearing (every
- *    partial is written before it is read); calls whose kernels overlap on
- *    the GPU (different streams, no ordering) race on it.
+ *    partial is written before it is read, and each call's plan launch sets
+ *    its merge counts to zero); calls whose kernels overlap on the GPU
+ *    (different streams, no ordering) race on it.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int pa_decode_noalloc(const pa_shape_t *shape, const void *q, const void *k_pool,

@@ -37,9 +37,14 @@
 //    HBM stream leaves room for.
 //  * At the end of an item the four states are merged in two steps through a
 //    small scratch area (warps 1 and 3 into 0 and 2, then 2 into 0; only the
-//    G rows that hold query heads) while the ring keeps filling; a sequence with a single split writes bf16 output
-//    directly, otherwise the (max, sum, acc) partials go to the workspace and
-//    decode_merge_kernel combines them.
+//    G rows that hold query heads) while the ring keeps filling; a sequence
+//    with a single split writes bf16 output directly, otherwise the (max,
+//    sum, acc) partials go to the workspace, and the split of a (sequence,
+//    KV head) that finishes last -- a per-(sequence, KV head) count taken
+//    with an atomic after a fence -- combines them there, its four consumer
+//    warps taking the G query heads between them.  No second kernel: the
+//    merges of early-finishing sequences overlap the other CTAs' streaming,
+//    and a batch whose sequences all fit one split pays nothing for them.
 #include <cuda.h>
 
 #include <algorithm>
@@ -52,7 +57,9 @@ namespace pa {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMergeWarp = kConsumerWarps + 1;  // after the producer warp
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kMergeSlots = 4;  // merge requests queued from the consumers to the merge warp
 constexpr int kQLane = 31;  // the producer lane that loads the items' query rows
 
 template <int D, int BS, bool FP8, bool BIG_G>
@@ -88,7 +95,11 @@ struct DecodeCfg {
     static constexpr int kQOff = kScratchOff + ((2 * kSlotFloats * 4 + 1023) / 1024) * 1024;
     static constexpr int kQHalves = D / 64;                // q is bf16: 64-column boxes of G rows
     static constexpr int kBarOff = kQOff + kQHalves * 2048;
-    static constexpr int kSmemBytes = kBarOff + (2 * kStages + 2) * 8 + 16 + 1024;
+    // barriers: ring full / empty, q full / empty, merge queue full / empty;
+    // then the abort flag (16 bytes) and the merge queue's slots
+    static constexpr int kNumBars = 2 * kStages + 2 + 2 * kMergeSlots;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + kMergeSlots * 16 + 1024;
+    static_assert((kNumBars * 8) % 16 == 0, "merge slots 16-byte aligned");
     // two: a third would need the registers cut to 128 (spills; measured slower)
     static constexpr int kCtasPerSm = 232448 / (kSmemBytes + 1024) < 2 ? 232448 / (kSmemBytes + 1024) : 2;
     static_assert(kStages >= kConsumerWarps && kStages < kQLane, "one producer lane per stage, and the q lane");
@@ -133,6 +144,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int *tmp, int *total) {
 }
 
 constexpr int kPlanBins = 256;  // last-split sizes (in blocks) sorted by a counting sort
+
+// Splits of a sequence of L > 0 tokens: ceil(L / split), but a last split of
+// at most split / 8 tokens joins the one before (so the step's new token
+// after a context of whole splits does not make an item, and a merge, of its
+// own).  Split c covers tokens [c split, (c + 1) split), the last one up to L.
+__device__ __forceinline__ int num_splits(int L, int split) {
+    const int ns = (L + split - 1) / split;
+    return (ns > 1 && L - (ns - 1) * split <= split / 8) ? ns - 1 : ns;
+}
 
 // The plan launch.  CTA 0 (1024 threads, thread t owns a contiguous range of
 // sequences): a sequence of L > 0 tokens has ns = ceil(L / split) splits;
@@ -183,25 +203,36 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     }
     const int per = (S + 1023) / 1024;
     const int s_beg = min(S, (int)threadIdx.x * per), s_end = min(S, s_beg + per);
-    // The tokens per split: the host's choice, or (split_adapt) the largest
-    // split_tokens * 2^k, k <= kSplitGrowth, that still leaves at least
-    // kMinItemsPerCta items per decode CTA and no item longer than half of a
-    // CTA's share of the batch's tokens.  Each item costs a fixed overhead
-    // (its query rows, the merge of the four warps' states) besides its
-    // blocks, so fewer, longer items are faster as long as the CTAs stay
-    // evenly loaded.
+    // The tokens per split: the host's choice, or (split_adapt) one of
+    // split_tokens * 2^k, k <= kSplitGrowth, from the batch's lengths:
+    //  1. no split at all (the smallest such k) when even the longest
+    //     sequence is at most 3/5 of a decode CTA's share of the batch's KV
+    //     blocks: the snake order then evens the items out, and a split only
+    //     adds items and merges;
+    //  2. otherwise the largest k that still leaves at least kMinItemsPerCta
+    //     items per CTA and no item longer than half of a CTA's share.
+    // Each item costs a fixed overhead (its query rows, the four warps'
+    // merge, the merge of its splits) besides its blocks, so fewer, longer
+    // items are faster as long as the CTAs stay evenly loaded.  (Fit to
+    // timings on GB300: 120 contexts U[1, 2048] run 20 % faster unsplit than
+    // in 512-token splits; 32 x 32K and a log-uniform [1, 8K] churn want
+    // rule 2.)
     int split = a.split_tokens;
     if (a.split_adapt) {
         constexpr int kSplitGrowth = 5, kMinItemsPerCta = 6;
-        long long cnt[kSplitGrowth + 1] = {}, tok = 0;
+        long long cnt[kSplitGrowth + 1] = {}, tok = 0, blk = 0;
+        int lmax = 0;
         for (int s = s_beg; s < s_end; ++s) {
             const int L = a.seq_lens[s];
             if (!len_ok(a, L, BS) || L == 0) continue;
             tok += L;
+            blk += (L + BS - 1) / BS;
+            lmax = max(lmax, L);
 #pragma unroll
             for (int k = 0; k <= kSplitGrowth; ++k) cnt[k] += (L + (split << k) - 1) / (split << k);
         }
-        __shared__ long long red[kSplitGrowth + 2][32];
+        __shared__ long long red[kSplitGrowth + 3][32];
+        __shared__ int red_max[32];
         auto block_sum = [&](long long v, int slot) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -210,22 +241,45 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int k = 0; k <= kSplitGrowth; ++k) block_sum(cnt[k], k);
         block_sum(tok, kSplitGrowth + 1);
+        block_sum(blk, kSplitGrowth + 2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+        if ((threadIdx.x & 31) == 0) red_max[threadIdx.x >> 5] = lmax;
+        __syncthreads();
+        // second level: warp w sums slot w (the next warp takes the maximum)
+        __shared__ long long tot[kSplitGrowth + 4];
+        {
+            const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+            if (w < kSplitGrowth + 3) {
+                long long v = red[w][l];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (l == 0) tot[w] = v;
+            } else if (w == kSplitGrowth + 3) {
+                int v = red_max[l];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+                if (l == 0) tot[w] = v;
+            }
+        }
         __syncthreads();
         __shared__ int chosen;
-        if (threadIdx.x < 32) {  // warp 0: the totals (lane k holds slot k), then the choice
-            long long t = 0;
-            if (threadIdx.x < kSplitGrowth + 2)
-                for (int w = 0; w < 32; ++w) t += red[threadIdx.x][w];
-            const long long tok_all = __shfl_sync(0xffffffffu, t, kSplitGrowth + 1);
+        if (threadIdx.x < 32) {  // warp 0, lane k: split_tokens << k
+            const int k = threadIdx.x;
             const long long ctas = max(a.num_ctas, 1);
-            const long long sp = (long long)a.split_tokens << threadIdx.x;
-            // lane k >= 1 qualifies if its split still leaves enough, short enough items
-            const bool fits = threadIdx.x >= 1 && threadIdx.x <= kSplitGrowth && t * Hkv >= kMinItemsPerCta * ctas &&
-                              sp * 2 * ctas <= tok_all * Hkv;
-            // the largest k such that every k' <= k qualifies
-            const unsigned bad = __ballot_sync(0xffffffffu, !fits && threadIdx.x >= 1 && threadIdx.x <= kSplitGrowth);
+            const long long tok_all = tot[kSplitGrowth + 1] * Hkv, blk_all = tot[kSplitGrowth + 2] * Hkv;
+            const long long lm = tot[kSplitGrowth + 3];
+            const long long sp = (long long)split << k;
+            const bool in_range = k <= kSplitGrowth;
+            // rule 1: the smallest k whose split holds the longest sequence
+            const bool small_longest = 5 * ((lm + BS - 1) / BS) * ctas <= 3 * blk_all;
+            const unsigned whole = __ballot_sync(0xffffffffu, in_range && sp >= lm);
+            // rule 2: the largest k such that every k' <= k qualifies
+            const bool fits = k >= 1 && in_range && (in_range ? tot[k] : 0) * Hkv >= kMinItemsPerCta * ctas &&
+                              sp * 2 * ctas <= tok_all;
+            const unsigned bad = __ballot_sync(0xffffffffu, !fits && k >= 1 && in_range);
             const int kmax = bad ? __ffs(bad) - 2 : kSplitGrowth;  // first failing k, minus one
-            if (threadIdx.x == 0) chosen = a.split_tokens << kmax;
+            if (k == 0) chosen = (small_longest && whole) ? split << (__ffs(whole) - 1) : split << kmax;
         }
         __syncthreads();
         split = chosen;
@@ -240,7 +294,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     for (int s = s_beg; s < s_end; ++s) {
         const int L = a.seq_lens[s];
         if (!len_ok(a, L, BS) || L == 0) continue;
-        const int ns = (L + split - 1) / split;
+        const int ns = num_splits(L, split);
         nfull += ns - 1;
         atomicAdd(&bins[key_of(L, ns)], 1);
     }
@@ -263,7 +317,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
                 for (int i = 0; i < a.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
             }
         } else {
-            const int ns = (L + split - 1) / split;
+            const int ns = num_splits(L, split);
             at = make_int2(pf, total_full + atomicAdd(&bins[key_of(L, ns)], 1));
             pf += ns - 1;
         }
@@ -271,13 +325,15 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     }
     __syncthreads();
     // Phase 2, a thread per (sequence, KV head), KV heads fastest: the items,
-    // so that neighbouring threads write neighbouring descriptors.
+    // so that neighbouring threads write neighbouring descriptors, and the
+    // merge count of every (sequence, KV head) set to zero.
     for (int p = threadIdx.x; p < S * Hkv; p += 1024) {
+        if (a.merge_cnt) a.merge_cnt[p] = 0;
         const int s = p / Hkv, g = p - s * Hkv;
         const int2 at = a.plan_seq[s];
         if (at.x < 0) continue;
         const int L = a.seq_lens[s];
-        const int ns = (L + split - 1) / split;
+        const int ns = num_splits(L, split);
         for (int c = 0; c < ns - 1; ++c) a.plan_items[(size_t)(at.x + c) * Hkv + g] = make_int4(s, g, c, L);
         a.plan_items[(size_t)at.y * Hkv + g] = make_int4(s, g, ns - 1, L);
     }
@@ -302,9 +358,9 @@ __device__ __forceinline__ Item load_item(const DecodeArgs &a, int k, int num_it
     it.g = v.y;
     it.c = v.z;
     it.L = v.w;
-    it.nsplit = it.valid ? (it.L + split - 1) / split : 1;
+    it.nsplit = it.valid ? num_splits(it.L, split) : 1;
     it.t0 = it.c * split;
-    it.t1 = min(it.L, it.t0 + split);
+    it.t1 = it.c == it.nsplit - 1 ? it.L : it.t0 + split;
     it.nblk = it.valid ? (it.t1 - it.t0 + BS - 1) / BS : 0;  // t0 is block aligned
     return it;
 }
@@ -324,7 +380,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
     uint64_t *empty = full + kS;
     uint64_t *q_full = empty + kS;
     uint64_t *q_empty = q_full + 1;
-    int *s_abort = reinterpret_cast<int *>(q_empty + 1);
+    uint64_t *mq_full = q_empty + 1;           // [kMergeSlots] a merge request is in slot i
+    uint64_t *mq_empty = mq_full + kMergeSlots;  // [kMergeSlots] the merge warp has taken slot i
+    int *s_abort = reinterpret_cast<int *>(mq_empty + kMergeSlots);
+    int4 *mq_slot = reinterpret_cast<int4 *>(s_abort + 4);  // (sequence, KV head, splits, -), or s < 0: no more
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -334,6 +393,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, kConsumerWarps);
+        for (int i = 0; i < kMergeSlots; ++i) {
+            mbar_init(&mq_full[i], 1);
+            mbar_init(&mq_empty[i], 1);
+        }
         // validation mode: skip everything if an earlier pass found a bad
         // index (read once, so that the whole CTA takes the same branch)
         *s_abort = (a.check_err_first && *(volatile int *)a.err != 0) ? 1 : 0;
@@ -422,6 +485,95 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
         return;
     }
 
+    // ------------------------------------------------------- merge warp --
+    // The split-K merge, in this kernel: for every item of a split sequence
+    // the consumers queue (sequence, KV head, splits) once its partials are
+    // stored; this warp counts the item in the (sequence, KV head)'s merge
+    // count with one acquire-release atomic, and the split that brings the
+    // count to the number of splits merges them all.  The consumers' partial
+    // stores reach the atomic through the queue's barrier (release / acquire
+    // in the CTA) and the atomic's release at GPU scope, which covers what
+    // this warp has observed; its acquire makes every other split's partials
+    // visible, and they are read from L2 (never L1, which can hold older
+    // copies of those lines).  The consumers never wait for any of this.
+    if (warp == kMergeWarp) {
+        const int G = a.group;
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int slot = n % kMergeSlots;
+            if (!mbar_wait(&mq_full[slot], (n / kMergeSlots) & 1, a.err)) {
+                atomicExch(s_abort, 1);
+                break;
+            }
+            const int4 req = mq_slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mq_empty[slot]);
+            if (req.x < 0) break;
+            const int s = req.x, g = req.y, nsplit = req.z;
+            uint32_t old = 0;
+            if (lane == 0) {
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(old)
+                             : "l"(a.merge_cnt + (size_t)s * a.num_kv_heads + g)
+                             : "memory");
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old != (uint32_t)(nsplit - 1)) continue;
+            // R rows of the group at a time, 32 / R lanes per row, CPL columns
+            // per lane: every lane's loads of a split are independent of the
+            // others', so a merge takes a few L2 round trips, not one per row.
+            const int R = G >= 8 ? 8 : (G >= 4 ? 4 : (G >= 2 ? 2 : 1));
+            const int lpr = 32 / R;           // lanes per row
+            const int cpl = D / lpr;          // columns per lane: 4 .. 32 (D = 128), 2 .. 16 (D = 64)
+            const int rl = lane / lpr, c0 = (lane % lpr) * cpl;
+            for (int rb = 0; rb < G; rb += R) {
+                const int row = rb + rl;
+                const bool live = row < G;
+                const size_t p0 = ((size_t)s * a.num_q_heads + g * G + (live ? row : 0)) * a.max_splits;
+                const float *ml = a.part_ml + p0 * 2;
+                float M = -INFINITY;
+#pragma unroll 8
+                for (int c = 0; c < nsplit; ++c) M = fmaxf(M, __ldcg(ml + c * 2));
+                float accv[32], lsum = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) accv[e] = 0.f;
+#pragma unroll 4
+                for (int c = 0; c < nsplit; ++c) {
+                    const float2 mlc = __ldcg(reinterpret_cast<const float2 *>(ml + c * 2));
+                    const float f = M == -INFINITY ? 0.f : fast_exp2(mlc.x - M);
+                    lsum += f * mlc.y;
+                    const float *pp = a.part_acc + (p0 + c) * D + c0;
+                    if (cpl == 2) {  // D = 64, one row per pass
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(pp));
+                        accv[0] += f * v.x;
+                        accv[1] += f * v.y;
+                    } else {
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            if (4 * e4 < cpl) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp) + e4);
+                                accv[4 * e4 + 0] += f * v.x;
+                                accv[4 * e4 + 1] += f * v.y;
+                                accv[4 * e4 + 2] += f * v.z;
+                                accv[4 * e4 + 3] += f * v.w;
+                            }
+                        }
+                    }
+                }
+                if (live) {
+                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                    __nv_bfloat16 *o = a.out + ((size_t)s * a.num_q_heads + g * G + row) * D + c0;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2)
+                        if (e < cpl)
+                            *reinterpret_cast<__nv_bfloat162 *>(o + e) =
+                                __floats2bfloat162_rn(accv[e] * inv, accv[e + 1] * inv);
+                }
+            }
+        }
+        return;
+    }
+
     // --------------------------------------------------------- consumers --
     // Byte offset of 16-byte chunk jj of token t in an fp8 K or V block (the
     // 128-byte swizzle XORs the chunk with the row's low three bits).
@@ -438,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
     const int cq = (lane & 3) * 2;  // first of the lane's two columns
     const uint32_t qb = smem_u32(qbuf);
     int base = 0;                   // the CTA-wide index of the item's first block
+    int nreq = 0;                   // merge requests queued (warp 0)
     bool ok = true;
     for (int j = 0;; ++j) {
         const Item it = item_at(j);
@@ -760,6 +913,22 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                 }
             }
         }
+        if (it.nsplit > 1 && warp == 0 && ok) {
+            // queue the merge request once the partials are stored (the
+            // barrier's arrival releases the warp's stores to the merge warp)
+            __syncwarp();
+            if (lane == 0) {
+                const int slot = nreq % kMergeSlots;
+                if (nreq < kMergeSlots || mbar_wait(&mq_empty[slot], ((nreq / kMergeSlots) - 1) & 1, a.err)) {
+                    mq_slot[slot] = make_int4(s, g, it.nsplit, 0);
+                    mbar_arrive(&mq_full[slot]);
+                } else {
+                    ok = false;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++nreq;
+        }
         // Every consumer warp takes the same barriers, and all leave together
         // once a wait has failed here or anywhere in the CTA: one barrier
         // reduction decides it for all (a flag read after a plain barrier
@@ -769,54 +938,16 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
             break;
         }
     }
-}
-
-// Combine the split partials of every (sequence, query head) with more than
-// one split: out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode kernel's partials
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.x * 4 + warp, s = blockIdx.y;
-    if (h >= a.num_q_heads) return;
-    if (a.check_err_first && *(volatile int *)a.err != 0) return;
-    const int L = a.seq_lens[s];
-    if (L < 0 || L > a.max_seq_len) return;
-    const int split = a.plan_count[1];  // the plan's choice
-    const int nsplit = L > 0 ? (L + split - 1) / split : 1;
-    if (nsplit <= 1) return;
-    const size_t p0 = ((size_t)s * a.num_q_heads + h) * a.max_splits;
-    const float *ml = a.part_ml + p0 * 2;
-    float M = -INFINITY;
-    for (int c = lane; c < nsplit; c += 32) M = fmaxf(M, ml[c * 2]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    constexpr int E = D / 32;  // elements per lane
-    float accv[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) accv[e] = 0.f;
-    float lsum = 0.f;
-    for (int c = 0; c < nsplit; ++c) {
-        const float f = fast_exp2(ml[c * 2] - M);
-        lsum += f * ml[c * 2 + 1];
-        const float *pa = a.part_acc + (p0 + c) * D + lane * E;
-        if constexpr (E == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(pa);
-            accv[0] += f * v.x;
-            accv[1] += f * v.y;
-            accv[2] += f * v.z;
-            accv[3] += f * v.w;
+    // no more merge requests: the merge warp leaves once it has taken this
+    if (warp == 0 && lane == 0) {
+        const int slot = nreq % kMergeSlots;
+        if (nreq < kMergeSlots || mbar_wait(&mq_empty[slot], ((nreq / kMergeSlots) - 1) & 1, a.err)) {
+            mq_slot[slot] = make_int4(-1, 0, 0, 0);
+            mbar_arrive(&mq_full[slot]);
         } else {
-            const float2 v = *reinterpret_cast<const float2 *>(pa);
-            accv[0] += f * v.x;
-            accv[1] += f * v.y;
+            atomicExch(s_abort, 1);
         }
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    __nv_bfloat16 *o = a.out + ((size_t)s * a.num_q_heads + h) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<__nv_bfloat162 *>(o + e) = __floats2bfloat162_rn(accv[e] * inv, accv[e + 1] * inv);
 }
 
 template <int D, int BS, bool BIG_G, bool FP8>
@@ -843,9 +974,9 @@ cudaError_t launch_decode_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, co
     decode_plan_kernel<D, BS><<<plan_ctas, 1024, 0, stream>>>(b);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // Programmatic dependent launches: each kernel's CTAs are placed while
-    // the previous one still runs and wait for it in griddepcontrol.wait, so
-    // the launch gaps between the three kernels overlap the work.
+    // Programmatic dependent launch: the decode kernel's CTAs are placed
+    // while the plan launch still runs and wait for it in griddepcontrol.wait,
+    // so the launch gap between the two overlaps the plan.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -856,12 +987,7 @@ cudaError_t launch_decode_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, co
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_splitk_kernel<D, BS, BIG_G, FP8>, tm_q, tm_k, tm_v, b);
-    if (e != cudaSuccess || b.max_splits <= 1) return e;
-    cfg.gridDim = dim3((b.num_q_heads + 3) / 4, b.num_seqs);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, b);
+    return cudaLaunchKernelEx(&cfg, decode_splitk_kernel<D, BS, BIG_G, FP8>, tm_q, tm_k, tm_v, b);
 }
 
 }  // namespace
@@ -885,7 +1011,8 @@ int decode_max_splits(int max_seq_len, int split_tokens) {
 
 // Layout: [part_acc S*Hq*max_splits*d floats][part_ml S*Hq*max_splits*2
 // floats] (only when max_splits > 1), then the plan, 16-byte aligned:
-// [items: S * max_splits * Hkv int4][count: 4 ints][per sequence: int2].
+// [items: S * max_splits * Hkv int4][count: 4 ints][per sequence: int2]
+// [merge counts: S * Hkv ints] (the last only when max_splits > 1).
 static size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int max_splits) {
     if (max_splits <= 1) return 0;
     const size_t n = (size_t)num_seqs * num_q_heads * max_splits;
@@ -895,16 +1022,18 @@ static size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int ma
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits) {
     return partials_bytes(num_seqs, num_q_heads, head_dim, max_splits) +
            (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4) + 4 * sizeof(int) +
-           (size_t)num_seqs * sizeof(int2);
+           (size_t)num_seqs * sizeof(int2) + (max_splits > 1 ? (size_t)num_seqs * num_kv_heads * sizeof(int) : 0);
 }
 
 void decode_plan_layout(void *ws, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits,
-                        int4 **items, int **count, int2 **seq) {
+                        int4 **items, int **count, int2 **seq, int **merge_cnt) {
     uint8_t *p = static_cast<uint8_t *>(ws) + partials_bytes(num_seqs, num_q_heads, head_dim, max_splits);
     *items = reinterpret_cast<int4 *>(p);
     p += (size_t)num_seqs * std::max(max_splits, 1) * num_kv_heads * sizeof(int4);
     *count = reinterpret_cast<int *>(p);
     *seq = reinterpret_cast<int2 *>(p + 4 * sizeof(int));
+    *merge_cnt = max_splits > 1 ? reinterpret_cast<int *>(p + 4 * sizeof(int) + (size_t)num_seqs * sizeof(int2))
+                                : nullptr;
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,

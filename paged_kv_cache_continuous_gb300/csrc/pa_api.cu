@@ -259,7 +259,7 @@ int do_decode(const pa_shape_t *sh, const void *q, const void *k_pool, const voi
                     ? static_cast<float *>(ws) + (size_t)num_seqs * sh->num_q_heads * max_splits * sh->head_dim
                     : nullptr;
     decode_plan_layout(ws, num_seqs, sh->num_q_heads, sh->num_kv_heads, sh->head_dim, max_splits, &a.plan_items,
-                       &a.plan_count, &a.plan_seq);
+                       &a.plan_count, &a.plan_seq, &a.merge_cnt);
     a.err = d->err;
     a.num_seqs = num_seqs;
     a.num_q_heads = sh->num_q_heads;

@@ -56,6 +56,10 @@ struct DecodeArgs {
     int4 *plan_items;
     int *plan_count;
     int2 *plan_seq;  // the plan's per-sequence scratch
+    // [S][Hkv] splits of each (sequence, KV head) done (null when nothing can
+    // split): set to zero by the plan launch; the split that brings it to the
+    // sequence's split count merges the partials.
+    int *merge_cnt;
 };
 
 // Tokens per split-K chunk chosen for a decode batch (multiple of block_size).
@@ -67,10 +71,10 @@ int decode_max_splits(int max_seq_len, int split_tokens);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits);
 // Where the plan lives inside that workspace.
 void decode_plan_layout(void *ws, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_splits,
-                        int4 **items, int **count, int2 **seq);
+                        int4 **items, int **count, int2 **seq, int **merge_cnt);
 
 // The plan launch (with the fused append's CTAs), then the persistent decode
-// kernel (and the merge when any sequence splits), all on `stream`.
+// kernel (which also merges the splits), both on `stream`.
 // tm_q: q as rows [S * Hq][d] bf16, boxes of 64 columns x G rows, 128-byte swizzle.
 cudaError_t launch_decode(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const DecodeArgs &a, int head_dim, int block_size, int num_sms, cudaStream_t stream,

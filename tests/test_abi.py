@@ -108,9 +108,10 @@ def _ws_bytes(S, Hq, Hkv, d, splits):
     """The documented workspace: split partials (fp32 acc and (max, sum) per
     sequence, query head and split, rounded up to 16 bytes; none for one
     split), then the plan's work items (16 bytes per sequence, split and KV
-    head), its 16 bytes of counters and 8 bytes per sequence."""
+    head), its 16 bytes of counters, 8 bytes per sequence and, when anything
+    can split, a merge count per sequence and KV head (4 bytes)."""
     partials = -(-(S * Hq * splits * (d + 2) * 4) // 16) * 16 if splits > 1 else 0
-    return partials + S * splits * Hkv * 16 + 16 + S * 8
+    return partials + S * splits * Hkv * 16 + 16 + S * 8 + (S * Hkv * 4 if splits > 1 else 0)
 
 
 def test_workspace_size(lib):

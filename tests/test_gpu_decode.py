@@ -73,6 +73,16 @@ def test_decode_ragged(cuda_lib, Hq, Hkv, d, B, split):
     _check_full(shape, kp, vp, st, f"G={Hq // Hkv} d={d} B={B} split={split}", split)
 
 
+@pytest.mark.parametrize("Hq,Hkv,d,B", [(32, 8, 128, 16), (64, 8, 128, 32), (8, 8, 64, 16)])
+def test_short_last_split_joins(cuda_lib, Hq, Hkv, d, B):
+    """With 256-token splits, a last split of at most 32 tokens joins the one
+    before (lengths k * 256 + 1 .. + 32), one of 33 or more is an item of its
+    own; every case, merged or not, against the oracle."""
+    lens = [257, 256 + 32, 256 + 33, 512 + 1, 512 + 16, 512 + 32, 512 + 33, 3 * 256 + 1, 256, 33]
+    shape, kp, vp, st = _ragged(12, lens, Hq, Hkv, d, B)
+    _check_full(shape, kp, vp, st, f"joined last split G={Hq // Hkv} d={d} B={B}", 256)
+
+
 def test_split_and_unsplit_agree(cuda_lib):
     shape, kp, vp, st = _ragged(8, [3000, 900, 64], 32, 8, 128, 16)
     outs = []
