@@ -612,35 +612,44 @@ def measure_fp8_decode(pa, wl, dev, hbm_peak, steps):
 
 
 def measure_serving(dev, chunking: bool):
-    """Closed-loop continuous batching (host scheduler + one pa_mixed_step per
-    step, mock activations): 512 requests arrive at once, prompts U[16, 512],
-    U[64, 256] new tokens each, Hq 32 / Hkv 8 / d 128, B 16; run until all
-    are done.  Wall-clock over the whole run (host planning, H2D of the step's
-    index arrays and the GPU step), and the GPU time of the steps alone."""
+    """Closed-loop continuous batching (host scheduler + one pa_mixed_step_split
+    per step, the SMs divided by the planned pair count when a step has both
+    prompts and decode rows; mock activations): 512 requests arrive at once,
+    prompts U[16, 512], U[64, 256] new tokens each, Hq 32 / Hkv 8 / d 128,
+    B 16; run until all are done.  Wall-clock over the whole run (host
+    planning, H2D of the step's index arrays and the GPU step), and the GPU
+    time of the steps alone (a second identical run, each step queued behind
+    a GPU sleep so that its events bracket device time only)."""
     from paged_kv_cache_continuous_gb300 import workload as wl
     from paged_kv_cache_continuous_gb300.serving import ServingLoop
     import time
-    shape = wl.Shape(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, num_blocks=26000)
-    loop = ServingLoop(shape, device=dev, seed=11, max_batch_prefill_tokens=4096, chunking=chunking,
-                       max_input_tokens=1024, max_total_tokens=2048, max_seqs=1024, max_tokens=8192)
-    rng = np.random.default_rng(12)
-    for i in range(512):
-        loop.submit(i, int(rng.integers(16, 513)), int(rng.integers(64, 257)))
-    torch.cuda.synchronize(dev)
-    loop.time_gpu = True
-    t0 = time.perf_counter()
-    while loop.step() is not None:
-        pass
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - t0
-    gpu = np.array(loop.gpu_ms())
+    def run(time_gpu):
+        shape = wl.Shape(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, num_blocks=26000)
+        loop = ServingLoop(shape, device=dev, seed=11, max_batch_prefill_tokens=4096, chunking=chunking,
+                           max_input_tokens=1024, max_total_tokens=2048, max_seqs=1024, max_tokens=8192)
+        rng = np.random.default_rng(12)
+        for i in range(512):
+            loop.submit(i, int(rng.integers(16, 513)), int(rng.integers(64, 257)))
+        torch.cuda.synchronize(dev)
+        loop.time_gpu = time_gpu
+        t0 = time.perf_counter()
+        while loop.step() is not None:
+            pass
+        torch.cuda.synchronize(dev)
+        return loop, time.perf_counter() - t0
+
+    # wall clock from a plain run; the device time of the steps from a second,
+    # identical (seeded) run that queues each step behind a GPU sleep
+    loop, wall = run(False)
+    loop_t, _ = run(True)
+    gpu = np.array(loop_t.gpu_ms())
     return {"requests": 512, "steps": loop.steps, "generated_tokens": loop.generated, "wall_s": round(wall, 4),
             "tokens_per_s": round(loop.generated / wall, 1), "ms_per_step": round(wall / loop.steps * 1e3, 4),
             "gpu_ms_per_step": round(float(gpu.mean()), 4), "gpu_s": round(float(gpu.sum()) / 1e3, 4),
             "tokens_per_gpu_s": round(loop.generated / (float(gpu.sum()) / 1e3), 1),
             "chunking": chunking,
-            "note": "wall clock includes host planning and Python marshalling; gpu_* is the pa_mixed_step "
-                    "device time (CUDA events) alone"}
+            "note": "wall clock includes host planning and Python marshalling; gpu_* is the step's device "
+                    "time (CUDA events around each pa_mixed_step queued behind a GPU sleep) alone"}
 
 
 def measure_long_context(pa, wl, dev, hbm_peak, iters):

@@ -34,7 +34,7 @@ class ServingLoop:
         self.finished = []
         self.prompt_len = {}
         self.last = None  # the last step's inputs (host numpy / device tensors), for checking
-        self.gpu_events = []  # (start, end) CUDA events around each step's pa_mixed_step, if timed
+        self.gpu_events = []  # (start, end) CUDA events around each step's pa_mixed_step, if timed (adds a GPU sleep per step)
         self.time_gpu = False
         self.partition = True  # pa_mixed_step_split on the planned pair count (False: pa_mixed_step)
 
@@ -63,13 +63,20 @@ class ServingLoop:
         max_len = int(plan["seq_lens"].max())
         if keep_inputs:
             self.last = dict(plan=plan, q=q, k=kn, v=vn, kp_before=self.kp.clone(), vp_before=self.vp.clone())
+        # The GPU's SMs are divided between the step's prefill and decode by
+        # the cost model, from the lengths the plan already holds on the host
+        # (only for steps that have both).
+        lens_h = plan["seq_lens"]
+        pairs = None
+        if self.partition and 0 < nd < len(rows):
+            pairs = pa.mixed_prefill_pairs(sh, lens_h[:nd], rows[nd:], lens_h[nd:] - rows[nd:])
         if self.time_gpu:
+            # A GPU sleep first, so that the step's launches are all queued
+            # when the start event is reached: the events then bracket the
+            # step's device time, not the host's enqueue of it.
+            torch.cuda._sleep(1_000_000)
             ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             ev[0].record()
-        # The GPU's SMs are divided between the step's prefill and decode by
-        # the cost model, from the lengths the plan already holds on the host.
-        lens_h = plan["seq_lens"]
-        pairs = pa.mixed_prefill_pairs(sh, lens_h[:nd], rows[nd:], lens_h[nd:] - rows[nd:]) if self.partition else None
         out = pa.mixed_step(sh, q, kn, vn, qs, lens, slots, bt, nd, max_len, max_q, self.kp, self.vp,
                             prefill_pairs=pairs)
         if self.time_gpu:
