@@ -158,8 +158,9 @@ __device__ __forceinline__ int num_splits(int L, int split) {
 // sequences): a sequence of L > 0 tokens has ns = ceil(L / split) splits;
 // items (s, g, c, L) go first for every sequence's ns - 1 full splits, then
 // for the last splits, longest first (counting sort on their length in
-// blocks; equal lengths in no fixed order -- each item writes its own
-// outputs, so the order changes no result).  Empty sequences get zero
+// blocks; equal lengths in no fixed order -- an item's result depends on the
+// item alone, since its four warps merge by item-local role, so the order
+// changes no bit of the output).  Empty sequences get zero
 // output here; a bad length sets the error word and gets no item.
 // CTAs 1.. (only with the append fused): row s of k_new / v_new, every KV
 // head, to slot_mapping[s] of the pools (16-byte pieces, grid-stride).
@@ -640,9 +641,13 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
         float l_run[2] = {0.f, 0.f};              // this lane's share of the row sums
         const float sl = FP8 ? a.scale_log2 * a.k_scale[g] : a.scale_log2;
 
-        // this warp's blocks: CTA-wide index = warp mod 4
-        for (int gi = base + (warp - base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-             ok && gi < base + nblk; gi += kConsumerWarps) {
+        // This warp's blocks: CTA-wide index = warp mod 4 (the stage's reader),
+        // i.e. the item's blocks i = role, role + 4, ...  The merge below goes
+        // by role, not by warp, so an item's result does not depend on where
+        // in the CTA's sequence of blocks it starts: the output is the same
+        // whatever CTA or list position the plan gives the item.
+        const int role = (warp - base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+        for (int gi = base + role; ok && gi < base + nblk; gi += kConsumerWarps) {
             const int i = gi - base;
             const int st = gi % kS;
             if (!mbar_wait(&full[st], (gi / kS) & 1, a.err)) {
@@ -864,16 +869,16 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                 : "memory");
             return r != 0u;
         };
-        // two steps: warps 1 and 3 into 0 and 2, then 2 into 0
+        // two steps: roles 1 and 3 into 0 and 2, then 2 into 0
         csync();  // every warp is done with the item; the previous merge's reads are done
-        if (warp & 1) put(warp >> 1);
+        if (role & 1) put(role >> 1);
         csync();
-        if (!(warp & 1)) take(warp >> 1);
+        if (!(role & 1)) take(role >> 1);
         csync();
-        if (warp == 2) put(0);
+        if (role == 2) put(0);
         csync();
-        if (warp == 0) take(0);
-        if (warp == 0) {
+        if (role == 0) take(0);
+        if (role == 0) {
             const float vs = FP8 ? a.v_scale[g] : 1.f;
 #pragma unroll
             for (int rr = 0; rr < (BIG_G ? 2 : 1); ++rr) {
@@ -913,10 +918,19 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
                 }
             }
         }
-        if (it.nsplit > 1 && warp == 0 && ok) {
-            // queue the merge request once the partials are stored (the
-            // barrier's arrival releases the warp's stores to the merge warp)
-            __syncwarp();
+        // Every consumer warp takes the same barriers, and all leave together
+        // once a wait has failed here or anywhere in the CTA: one barrier
+        // reduction decides it for all (a flag read after a plain barrier
+        // could change between the warps' reads).
+        if (csync_any(!ok || *(volatile int *)s_abort != 0)) {
+            if (!ok) atomicExch(s_abort, 1);
+            break;
+        }
+        if (it.nsplit > 1 && warp == 0) {
+            // Queue the merge request (always from warp 0, which counts the
+            // queue's slots): the partials were stored by the role-0 warp
+            // before the barrier above, and the slot's arrival releases them
+            // to the merge warp.
             if (lane == 0) {
                 const int slot = nreq % kMergeSlots;
                 if (nreq < kMergeSlots || mbar_wait(&mq_empty[slot], ((nreq / kMergeSlots) - 1) & 1, a.err)) {
@@ -928,14 +942,6 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, BS, FP8, BIG_G>::kCtasP
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             ++nreq;
-        }
-        // Every consumer warp takes the same barriers, and all leave together
-        // once a wait has failed here or anywhere in the CTA: one barrier
-        // reduction decides it for all (a flag read after a plain barrier
-        // could change between the warps' reads).
-        if (csync_any(!ok || *(volatile int *)s_abort != 0)) {
-            if (!ok) atomicExch(s_abort, 1);
-            break;
         }
     }
     // no more merge requests: the merge warp leaves once it has taken this

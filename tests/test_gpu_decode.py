@@ -310,3 +310,21 @@ def test_llama7b_decode_append_full_size_sampled(cuda_lib):
     ref = oracle.decode(bits(st.q)[seqs], kc, vc, bt, st.seq_lens[seqs], pairs=pairs)
     got = out[torch.tensor(seqs[pairs[:, 0]]), torch.tensor(pairs[:, 1])]
     assert_close(got, ref, "Llama-7B decode_append")
+
+
+@pytest.mark.parametrize("split", [0, 64])
+def test_decode_bitwise_repeatable(cuda_lib, split):
+    """An item's result depends on the item alone (its warps merge by
+    item-local role; a split sequence's partials are merged in split order),
+    so repeated calls -- whose plans may order equal-length items
+    differently -- give the same bits."""
+    shape, kp, vp, st = _ragged(13, LENS * 6, 32, 8, 128, 16)
+    kd, vd = _append_gpu(shape, kp, vp, st)
+    pa.set_decode_split(split)
+    try:
+        outs = [_decode_gpu(shape, kd, vd, st).clone() for _ in range(5)]
+        pa.check_device_error()
+    finally:
+        pa.set_decode_split(0)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])

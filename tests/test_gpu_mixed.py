@@ -162,3 +162,24 @@ def test_mixed_split_full_size_planned(cuda_lib):
     kh, vh = oracle.kv_append(bits(st.k_new), bits(st.v_new), st.slot_mapping, bits(kp), bits(vp))
     assert np.array_equal(bits(kd), kh) and np.array_equal(bits(vd), vh)
     _sampled_step_check(shape, st, out, kd, vd, np.random.default_rng(6), "mixed split full", host_pool=(kh, vh))
+
+
+def test_mixed_split_decode_rows_bitexact(cuda_lib):
+    """With the decode split fixed, the partitioned step's decode rows equal
+    the undivided step's bit for bit: the decode grid differs (fewer CTAs)
+    but an item's result does not depend on the CTA that runs it."""
+    shape, kp, vp, st = wl.mixed(seed=35, num_decode=40, num_prompts=4, prompt_range=(100, 500),
+                                 prefill_budget=1600, max_context=1500)
+    nd = st.num_decode
+    args = (shape, dev(st.q), dev(st.k_new), dev(st.v_new), dev(st.q_start_loc), dev(st.seq_lens),
+            dev(st.slot_mapping), dev(st.block_table), nd, st.max_seq_len, st.max_q_len)
+    pa.set_decode_split(256)
+    try:
+        kd, vd = dev(kp), dev(vp)
+        out1 = pa.mixed_step(*args, kd, vd, prefill_pairs=20)
+        kd2, vd2 = dev(kp), dev(vp)
+        out2 = pa.mixed_step(*args, kd2, vd2)
+        pa.check_device_error()
+    finally:
+        pa.set_decode_split(0)
+    assert torch.equal(out1, out2)
