@@ -234,8 +234,10 @@ int pa_mixed_step(const pa_shape_t *shape, const void *q, const void *k_new,
  * tensor-core pair kernel (head_dim 128) and 2 * prefill_pairs is below the
  * device's SM count; otherwise the step runs as pa_mixed_step.  The appended
  * pools and the prefill rows are bit for bit pa_mixed_step's (a prefill work
- * unit is summed the same way on any pair); the decode rows agree within the
- * decode's tolerance, since its split-K factor is chosen for the SMs it gets.
+ * unit is summed the same way on any pair); so are the decode rows when both
+ * use the same split-K factor (pa_set_decode_split), and otherwise they agree
+ * within the decode's tolerance: the plan chooses the factor for the SMs the
+ * decode gets.
  * A negative count is PA_ERR_INVALID_ARG.  pa_mixed_prefill_pairs gives a
  * count for a step.
  */
