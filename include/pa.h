@@ -147,7 +147,9 @@ int pa_kv_append(const pa_shape_t *shape, const void *k_new, const void *v_new,
  * Long contexts are split into chunks (split-K) whose partial softmax states
  * are merged in the same kernel, by the chunk of each (sequence, KV head)
  * that finishes last; the split is chosen from max_seq_len, which must bound
- * every seq_lens[s] (a longer sequence sets the device error word).
+ * every seq_lens[s] (a longer sequence sets the device error word).  The
+ * output is bitwise repeatable: for the same inputs and split it does not
+ * depend on the order or the CTA in which the work items run.
  * workspace: at least pa_workspace_size(shape, num_seqs, max_seq_len) bytes.
  */
 int pa_decode(const pa_shape_t *shape, const void *q, const void *k_pool,
