@@ -502,7 +502,12 @@ int pa_rope_append(const pa_shape_t *shape, const void *q, const void *k_new, co
     a.num_blocks = shape->num_blocks;
     a.check_err_first = val;
     const double theta = rope_theta == 0.f ? 10000.0 : (double)rope_theta;
-    for (int i = 0; i < shape->head_dim / 2; ++i) a.inv_freq[i] = pow(theta, -2.0 * i / shape->head_dim);
+    for (int i = 0; i < shape->head_dim / 2; ++i) {
+        // the frequency in turns per position, its fractional part as 64-bit fixed point
+        double q = pow(theta, -2.0 * i / shape->head_dim) / 6.283185307179586;
+        q -= std::floor(q);
+        a.turn[i] = q >= 1.0 ? 0ull : (unsigned long long)std::ldexp(q, 64);
+    }
     cudaError_t e = launch_rope_append(a, d->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope_append launch");
     return ok();

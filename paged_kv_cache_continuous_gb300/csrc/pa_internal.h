@@ -103,7 +103,9 @@ struct RopeArgs {
     int *err;
     int num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
     int check_err_first;
-    double inv_freq[64];  // theta^(-2i/d), i < d/2
+    // turn[i]: f_i / (2 pi) as a 64-bit fixed-point fraction of a turn, with
+    // f_i = theta^(-2i/d), i < d/2; position p's angle is p * turn[i] mod 2^64
+    unsigned long long turn[64];
 };
 cudaError_t launch_rope_append(const RopeArgs &a, int num_sms, cudaStream_t stream);
 

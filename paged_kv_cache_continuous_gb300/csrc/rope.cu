@@ -9,9 +9,11 @@
 // of length d at position p and i < d/2, with f_i = theta^(-2i/d),
 //     y[i]       = x[i] cos(p f_i) - x[i + d/2] sin(p f_i)
 //     y[i + d/2] = x[i + d/2] cos(p f_i) + x[i] sin(p f_i).
-// The frequencies come from the host in double; p f_i is formed and reduced
-// modulo 2 pi in double, so cos / sin are taken (in float) of an angle in
-// [-pi, pi] whatever the position; the rotation is float, rounded to bf16.
+// The host gives each frequency as a 64-bit fixed-point fraction of a turn,
+// f_i / (2 pi) (from its double value); p times it modulo 2^64 is the angle's
+// part of a turn, exact in integer arithmetic, so cos / sin are taken (in
+// float) of an angle in [-pi, pi) whatever the position, with no FP64 work;
+// the rotation is float, rounded to bf16.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -98,10 +100,13 @@ __global__ void __launch_bounds__(kThreads)
                 for (int e = threadIdx.x; e < nt * half; e += kThreads) {
                     const int tt = e / half, i = e % half;
                     const int p = __ldg(a.positions + t0 + tt);
-                    double ang = (double)max(p, 0) * a.inv_freq[i];
-                    ang -= rint(ang * 0.15915494309189535) * 6.283185307179586;  // into [-pi, pi]
+                    // p f_i in turns, modulo whole turns: exact integer arithmetic
+                    // (no FP64, a slow pipe on this GPU); the top 32 bits read as a
+                    // signed fraction of a turn give the angle in [-pi, pi).
+                    const unsigned long long tr = (unsigned long long)(unsigned)max(p, 0) * a.turn[i];
+                    const float ang = (float)(int)(unsigned)(tr >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
                     float sn, cn;
-                    sincosf((float)ang, &sn, &cn);
+                    sincosf(ang, &sn, &cn);
                     cs[tt][i + (i >> 3)] = make_float2(cn, sn);
                     if (i == 0) {
                         const int sl = __ldg(a.slot_mapping + t0 + tt);
