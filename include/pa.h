@@ -30,7 +30,9 @@
  * Conventions shared by every call
  * ---------------------------------------------------------------------------
  *  - Pointers named q, k*, v*, out, *_pool, workspace and every int32 index
- *    array are DEVICE pointers; the caller owns all of them.  The library
+ *    array are DEVICE pointers (except the host-side planners:
+ *    pa_mixed_prefill_pairs here, and pa_alloc.h / pa_sched.h, whose arrays
+ *    are host memory); the caller owns all of them.  The library
  *    calls no cudaMalloc.  The state it does keep, all process-wide:
  *      - the validation flag, the decode split override and the prefill
  *        CTA-pair override (pa_set_validation, pa_set_decode_split,
