@@ -27,3 +27,25 @@ def test_reference_arm_json_line():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_decode_step_bytes_split_rule():
+    """The decode's algorithmic bytes count split partials by the documented
+    split rule: ceil(L / split) splits, one fewer when the last would hold at
+    most split / 8 tokens; partials only for sequences with two or more."""
+    import numpy as np
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    class Sh:
+        num_q_heads, num_kv_heads, head_dim = 8, 2, 64
+
+    lens = np.array([256, 257, 256 + 32, 256 + 33, 512 + 32, 512 + 33, 1], dtype=np.int32)
+    nsplit = np.array([1, 1, 1, 2, 2, 3, 1])
+    got = bench.decode_step_bytes(Sh, lens, 256, 16)
+    L = lens.astype(np.int64)
+    kv = int(L.sum()) * 2 * 64 * 2 * 2
+    qo = 2 * 7 * 8 * 64 * 2
+    tables = int(np.ceil(L / 16).sum()) * 4 + 7 * 4
+    partials = int(nsplit[nsplit > 1].sum()) * 8 * (64 + 2) * 4 * 2
+    assert got["decode"] == kv + qo + tables + partials
